@@ -1,0 +1,191 @@
+"""Seeded synthetic inputs for MLA decode: the only code shared by the CUDA path's
+tests/benchmark and the oracle's tests.  It draws tensors and builds block
+tables; it contains none of the attention arithmetic.
+
+Recipe (all draws from fresh ``torch.Generator`` objects, one per tensor, seeded
+``1000 * seed + k`` for the k-th tensor of the list below, so every tensor is
+reproducible on its own; the ragged lengths come first, from a generator seeded
+``seed`` itself):
+
+  --   sequence lengths (ragged workload only): ``randint(lo, hi + 1)``
+  k=1  cache rows   ~ N(0, 1) * 0.5, rounded to bf16 (round-to-nearest-even)
+  k=2  q_abs        ~ N(0, 1) * 0.5, bf16
+  k=3  q_nope       ~ N(0, 1) * 0.5, bf16
+  k=4  q_rope       ~ N(0, 1) * 0.5, bf16
+  k=5  W_UK         ~ N(0, 1) / sqrt(512), bf16   (standard deviation 1/sqrt(512))
+  k=6  W_UV         ~ N(0, 1) / sqrt(512), bf16
+  k=7  block-table permutation of the page pool (shuffled layouts)
+  k=8  choice of the peaked rows (1% of each sequence's rows scaled by 8 before
+       the bf16 rounding)
+  --   optional garbage (NaN or 1e30) written into pool pages and tail slots that
+       no sequence may read
+
+Shapes follow the DeepSeek-V2 attention: 128 heads, 512-d latent, 64-d decoupled
+RoPE key, 128-d head, 576-number cache row, 64-token pages.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import torch
+
+H = 128
+D_C = 512
+D_R = 64
+D_H = 128
+D = D_C + D_R
+PAGE = 64
+SCALE = 1.0 / math.sqrt(D_H + D_R)
+
+
+@dataclass
+class Case:
+    name: str
+    B: int
+    Tq: int
+    causal: bool
+    seq_lens: torch.Tensor          # [B] int32 (CPU)
+    block_table: torch.Tensor       # [B, max_pages] int32 (CPU), -1 padded
+    pool: torch.Tensor              # [num_pages, PAGE, D] bf16
+    q_abs: Optional[torch.Tensor] = None   # [B, Tq, H, D] bf16
+    q_nope: Optional[torch.Tensor] = None  # [B, Tq, H, D_H] bf16
+    q_rope: Optional[torch.Tensor] = None  # [B, Tq, H, D_R] bf16
+    w_uk: Optional[torch.Tensor] = None    # [H, D_H, D_C] bf16
+    w_uv: Optional[torch.Tensor] = None    # [H, D_H, D_C] bf16
+    scale: float = SCALE
+    meta: Dict = field(default_factory=dict)
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.pool.shape[0])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def cache_bytes(self) -> int:
+        """Bytes of latent cache one decode step must read (each visible row once)."""
+        return int(self.seq_lens.to(torch.int64).sum()) * D * 2
+
+
+def _gen(seed: int, k: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000 + k)
+    return g
+
+
+def _randn_bf16(shape, std: float, seed: int, k: int, device) -> torch.Tensor:
+    x = torch.randn(shape, generator=_gen(seed, k, device), device=device, dtype=torch.float32)
+    return (x * std).to(torch.bfloat16)
+
+
+def make_case(name: str, seq_lens: List[int], Tq: int = 1, causal: bool = False,
+              shuffle: bool = False, spare_pages: int = 0, garbage: Optional[str] = None,
+              peaked_frac: float = 0.0, q_mode: str = "abs", seed: int = 0,
+              device="cpu") -> Case:
+    """Build one synthetic decode problem.
+
+    seq_lens     cached tokens per sequence (includes the Tq new tokens when causal).
+    shuffle      place pages by a seeded random permutation of the pool (else in order).
+    spare_pages  extra pool pages no sequence owns.
+    garbage      None, "nan" or "big": fill the unowned pages and the unused tail slots
+                 of every sequence's last page with NaN or 1e30, to prove they are never read.
+    peaked_frac  fraction of each sequence's rows multiplied by 8 (whole 576-wide row).
+    q_mode       "abs": draw q_abs; "nope": draw q_nope, q_rope, W_UK, W_UV; "both".
+    """
+    device = torch.device(device)
+    B = len(seq_lens)
+    lens = torch.tensor(seq_lens, dtype=torch.int32)
+    pages_per = [(int(L) + PAGE - 1) // PAGE for L in seq_lens]
+    owned = sum(pages_per)
+    num_pages = max(1, owned + spare_pages)
+    max_pages = max(1, max(pages_per) if pages_per else 1)
+
+    if shuffle:
+        perm = torch.randperm(num_pages, generator=_gen(seed, 7, "cpu")).to(torch.int32)
+    else:
+        perm = torch.arange(num_pages, dtype=torch.int32)
+    block_table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    cursor = 0
+    for b in range(B):
+        n = pages_per[b]
+        block_table[b, :n] = perm[cursor:cursor + n]
+        cursor += n
+
+    base = torch.randn((num_pages, PAGE, D), generator=_gen(seed, 1, device), device=device,
+                       dtype=torch.float32) * 0.5
+    if peaked_frac > 0.0:
+        # scale whole rows by 8 before the bf16 rounding
+        g = _gen(seed, 8, "cpu")
+        mask = torch.zeros((num_pages, PAGE), dtype=torch.bool)
+        for b in range(B):
+            L = int(seq_lens[b])
+            k = int(math.floor(peaked_frac * L))
+            if k == 0:
+                continue
+            rows = torch.randperm(L, generator=g)[:k]
+            pg = block_table[b, (rows // PAGE)].to(torch.int64)
+            mask[pg, (rows % PAGE)] = True
+        base[mask.to(device)] *= 8.0
+    pool = base.to(torch.bfloat16)
+    del base
+
+    if garbage is not None:
+        val = float("nan") if garbage == "nan" else 1e30
+        used = torch.zeros((num_pages, PAGE), dtype=torch.bool)
+        for b in range(B):
+            L = int(seq_lens[b])
+            n = pages_per[b]
+            if n == 0:
+                continue
+            pg = block_table[b, :n].to(torch.int64)
+            used[pg[:-1], :] = True
+            used[pg[-1], : L - (n - 1) * PAGE] = True
+        pool[(~used).to(device)] = val
+
+    case = Case(name=name, B=B, Tq=Tq, causal=causal, seq_lens=lens, block_table=block_table,
+                pool=pool)
+    if q_mode in ("abs", "both"):
+        case.q_abs = _randn_bf16((B, Tq, H, D), 0.5, seed, 2, device)
+    if q_mode in ("nope", "both"):
+        case.q_nope = _randn_bf16((B, Tq, H, D_H), 0.5, seed, 3, device)
+        case.q_rope = _randn_bf16((B, Tq, H, D_R), 0.5, seed, 4, device)
+        case.w_uk = _randn_bf16((H, D_H, D_C), 1.0 / math.sqrt(D_C), seed, 5, device)
+        case.w_uv = _randn_bf16((H, D_H, D_C), 1.0 / math.sqrt(D_C), seed, 6, device)
+    case.meta = dict(seed=seed, shuffle=shuffle, spare_pages=spare_pages, garbage=garbage,
+                     peaked_frac=peaked_frac)
+    return case
+
+
+def ragged_lengths(B: int, lo: int, hi: int, seed: int = 0) -> List[int]:
+    """Lengths uniform in [lo, hi], drawn first from a generator seeded `seed`."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (B,), generator=g)]
+
+
+# ---------------------------------------------------------------------------
+# The five workloads (full size).  Names describe the workload, not an index.
+# ---------------------------------------------------------------------------
+WORKLOADS = {
+    # batch 1, 512-token contiguous cache (identity block table), naive-vs-absorbed check
+    "b1_l512": dict(seq_lens=[512], q_mode="both"),
+    # batch 64 x 4096 tokens, pages in order
+    "b64_l4096": dict(seq_lens=[4096] * 64),
+    # batch 128, lengths uniform in [1, 32768], shuffled block table over one pool
+    "b128_ragged32k": dict(ragged=(128, 1, 32768), shuffle=True),
+    # batch 8 x 131072 tokens, 1% of rows scaled x8 (peaked softmax rows)
+    "b8_l128k_peaked": dict(seq_lens=[131072] * 8, peaked_frac=0.01),
+    # batch 32, 4 causal query tokens over 8192 prior + 4 new tokens; fused absorb/up-proj
+    "b32_tq4_causal_fused": dict(seq_lens=[8192 + 4] * 32, Tq=4, causal=True, q_mode="both"),
+}
+
+
+def make_workload(name: str, seed: int = 0, device="cpu") -> Case:
+    spec = dict(WORKLOADS[name])
+    if "ragged" in spec:
+        B, lo, hi = spec.pop("ragged")
+        spec["seq_lens"] = ragged_lengths(B, lo, hi, seed)
+    return make_case(name, seed=seed, device=device, **spec)

@@ -1,0 +1,189 @@
+"""MLA oracle: slow, obviously-correct fp64 CPU reference.
+
+TEST INFRASTRUCTURE ONLY.  Imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``; the
+CUDA library and its Python binding never import, load or call anything here.
+
+The arithmetic lives in ``mla_oracle.c`` (compiled to ``liboracle.so`` by
+:func:`build`); this module only marshals numpy arrays.  Inputs are converted
+to float32 (bf16 values are exact in float32); every result is float64.
+
+Sources (see the C file for the passage each function follows):
+  * "DeepSeek-V2" explainer, Steps 5-8 (latent cache, absorption, decoupled
+    RoPE, 576-number cache row);
+  * DeepSeek-V2 paper breakdown, "How It Works" (latent c_t cached, up-projected
+    to K and V, separate RoPE key kept beside it).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (fp64, no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+               "-fno-fast-math", "-o", _LIB_PATH, _SRC, "-lm"]
+        subprocess.check_call(cmd)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.oracle_absorb_q.argtypes = [_f32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, _f64p]
+        lib.oracle_up_proj.argtypes = [_f64p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, _f64p]
+        lib.oracle_decode_absorbed.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _f32p, _i32p, _i32p,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_int, ctypes.c_int, _f64p, _f64p]
+        lib.oracle_decode_naive.argtypes = [_f32p, _f32p, _f32p, _f32p, _f32p, _i32p, _i32p,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int, ctypes.c_int, _f64p, _f64p]
+        lib.oracle_combine.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_long, ctypes.c_int,
+                                       _f64p, _f64p]
+        for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed",
+                   "oracle_decode_naive", "oracle_combine"):
+            getattr(lib, fn).restype = None
+        _lib = lib
+    return _lib
+
+
+def _f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor (bf16 -> f32 is exact)
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def absorb_q(q_nope, q_rope, w_uk) -> np.ndarray:
+    """q_abs[n,h] = [W_UK[h]^T q_nope[n,h] | q_rope[n,h]]  (Step 6 absorption, Step 7 RoPE part).
+
+    q_nope [..., H, d_h], q_rope [..., H, d_r], w_uk [H, d_h, d_c] -> [..., H, d_c + d_r] float64.
+    """
+    qn, qr, w = _f32(q_nope), _f32(q_rope), _f32(w_uk)
+    H, d_h, d_c = w.shape
+    lead = qn.shape[:-2]
+    N = int(np.prod(lead)) if lead else 1
+    d_r = qr.shape[-1]
+    out = np.zeros(lead + (H, d_c + d_r), dtype=np.float64)
+    if qr.size == 0:
+        qr = np.zeros(1, dtype=np.float32)
+    _load().oracle_absorb_q(qn, qr, w, N, H, d_h, d_c, d_r, out)
+    return out
+
+
+def up_proj(o_lat, w_uv) -> np.ndarray:
+    """out[n,h] = W_UV[h] o_lat[n,h]  (Step 5 value regeneration, applied after attention)."""
+    o, w = _f64(o_lat), _f32(w_uv)
+    H, d_h, d_c = w.shape
+    lead = o.shape[:-2]
+    N = int(np.prod(lead)) if lead else 1
+    out = np.zeros(lead + (H, d_h), dtype=np.float64)
+    _load().oracle_up_proj(o, w, N, H, d_h, d_c, out)
+    return out
+
+
+def decode_absorbed(q_abs, pool, block_table, seq_lens, scale: float, causal: bool = False,
+                    d_c: int = 512, nthreads: int | None = None):
+    """Absorbed decode over a paged latent cache.
+
+    q_abs [B, Tq, H, D] (float32-exact or float64), pool [P, page, D], block_table [B, max_pages],
+    seq_lens [B].  Returns (o_lat [B,Tq,H,d_c] float64, lse [B,Tq,H] float64).
+    """
+    pl = _f32(pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    if hasattr(q_abs, "detach") or np.asarray(q_abs).dtype != np.float64:
+        q32, q64 = _f32(q_abs), None
+        q = q32
+    else:
+        q32, q64 = None, _f64(q_abs)
+        q = q64
+    B, Tq, H, D = q.shape
+    page = pl.shape[1]
+    d_r = D - d_c
+    max_pages = bt.shape[1]
+    o = np.zeros((B, Tq, H, d_c), dtype=np.float64)
+    lse = np.zeros((B, Tq, H), dtype=np.float64)
+    if nthreads is None:
+        nthreads = default_threads()
+    _load().oracle_decode_absorbed(
+        q32.ctypes.data if q32 is not None else None,
+        q64.ctypes.data if q64 is not None else None,
+        pl, bt, sl, B, Tq, H, d_c, d_r, page, max_pages, float(scale), int(bool(causal)),
+        int(nthreads), o, lse)
+    return o, lse
+
+
+def decode_naive(q_nope, q_rope, w_uk, w_uv, pool, block_table, seq_lens, scale: float,
+                 causal: bool = False, nthreads: int | None = None):
+    """Naive MHA over per-head keys/values rebuilt from the latent cache.
+
+    q_nope [B,Tq,H,d_h], q_rope [B,Tq,H,d_r], w_uk/w_uv [H,d_h,d_c].
+    Returns (out [B,Tq,H,d_h] float64, lse [B,Tq,H] float64).
+    """
+    qn, qr, wk, wv, pl = _f32(q_nope), _f32(q_rope), _f32(w_uk), _f32(w_uv), _f32(pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    B, Tq, H, d_h = qn.shape
+    d_r = qr.shape[-1]
+    d_c = wk.shape[2]
+    page = pl.shape[1]
+    max_pages = bt.shape[1]
+    out = np.zeros((B, Tq, H, d_h), dtype=np.float64)
+    lse = np.zeros((B, Tq, H), dtype=np.float64)
+    if qr.size == 0:
+        qr = np.zeros(1, dtype=np.float32)
+    if nthreads is None:
+        nthreads = default_threads()
+    _load().oracle_decode_naive(qn, qr, wk, wv, pl, bt, sl, B, Tq, H, d_h, d_c, d_r, page,
+                                max_pages, float(scale), int(bool(causal)), int(nthreads), out, lse)
+    return out, lse
+
+
+def combine(o_parts, lse_parts):
+    """Merge attention results over disjoint token sets.
+
+    o_parts [R, ..., d], lse_parts [R, ...] -> (o [..., d], lse [...]) float64.
+    """
+    o = _f64(o_parts)
+    l = _f64(lse_parts)
+    R = o.shape[0]
+    d = o.shape[-1]
+    M = int(np.prod(o.shape[1:-1])) if o.ndim > 2 else 1
+    out = np.zeros(o.shape[1:], dtype=np.float64)
+    lse = np.zeros(l.shape[1:], dtype=np.float64)
+    _load().oracle_combine(o, l, R, M, d, out, lse)
+    return out, lse
