@@ -1,0 +1,364 @@
+"""Benchmark: MLA decode tokens/s and fraction of roofline on B300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one `mla_decode` call (split plan + decode kernel + LSE combine) over one
+batch of synthetic queries against a resident paged latent cache.  Default workload:
+batch 64, 4096-token contexts, 128 heads, 576-wide bf16 rows in 64-token pages.
+`value` is device-timed whole-job throughput (query tokens / s) with inputs resident in
+HBM; `e2e` is the same metric through the C ABI with host buffers (queries copied in,
+latent output and LSE copied out every step).  `--impl reference` times the fp64 CPU
+oracle (the only reference implementation there is) on a bounded sample of the same
+workload.  Multi-GPU (torchrun): every rank decodes its own batch (weak scaling), no
+collective on the data path; the barrier and max-over-ranks only bracket the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=64 H=128 L=4K"
+UNIT = "tokens/s"
+ROW_BYTES = 576 * 2
+FLOP_PER_TOKEN_QUERY = 2 * 128 * (576 + 512)
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_77_b300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(case, budget_s: float = 12.0, max_seqs: int = None):
+    """Time the fp64 oracle (absorbed form, all host cores) on a bounded sample of whole
+    sequences of the workload; returns (tokens/s, cores, sample description)."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import sub_problem
+    cores = oracle.default_threads()
+    B = case.B
+    # calibrate on one sequence, then size the sample to the budget
+    q, pool, bt, lens = sub_problem(case, [0])
+    t0 = time.perf_counter()
+    oracle.decode_absorbed(q, pool, bt, lens, case.scale, causal=case.causal, nthreads=cores)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(B if max_seqs is None else max_seqs, int(budget_s / max(t1, 1e-3))))
+    seqs = list(range(1, 1 + n)) if n + 1 <= B else list(range(n))
+    seqs = [s % B for s in seqs]
+    q, pool, bt, lens = sub_problem(case, seqs)
+    t0 = time.perf_counter()
+    oracle.decode_absorbed(q, pool, bt, lens, case.scale, causal=case.causal, nthreads=cores)
+    dt = time.perf_counter() - t0
+    toks = n * case.Tq
+    return toks / dt, cores, f"{n} of {B} sequences x {case.Tq} query tokens x 128 heads ({dt:.1f} s)"
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each step
+    decodes a bounded sample (`--ref-seqs` whole sequences, all heads and query tokens) of
+    the same workload; rank 0 alone runs it under torchrun."""
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    from mla_latent_kv_77_b300 import workloads
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import sub_problem
+    spec = dict(workloads.WORKLOADS[args.workload])
+    if "ragged" in spec:
+        Bf, lo, hi = spec.pop("ragged")
+        spec["seq_lens"] = workloads.ragged_lengths(Bf, lo, hi, 0)
+    full_B = len(spec["seq_lens"])
+    n = min(args.ref_seqs, full_B)
+    spec["seq_lens"] = spec["seq_lens"][:n]          # the sample: the first n sequences
+    case = workloads.make_case(args.workload, seed=0, device="cpu", **spec)
+    if case.q_abs is None:
+        case.q_abs = oracle.absorb_q(case.q_nope, case.q_rope, case.w_uk)
+    q, pool, bt, lens = sub_problem(case, list(range(n)))
+    cores = oracle.default_threads()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.decode_absorbed(q, pool, bt, lens, case.scale, causal=case.causal, nthreads=cores)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    toks = n * case.Tq
+    value = toks * len(times) / sum(times)
+    sample = f"{n} of {full_B} sequences x {case.Tq} query tokens x 128 heads per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "batch": full_B, "q_len": case.Tq, "heads": 128,
+                       "context": int(max(spec["seq_lens"])), "page": 64},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="b64_l4096")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seqs", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import mla_latent_kv_77_b300 as mla
+    from mla_latent_kv_77_b300 import build as mla_build, workloads
+    mla_build.build()
+
+    # every rank decodes its own batch of the workload (seed offset by rank)
+    case = workloads.make_workload(args.workload, seed=rank, device=dev)
+    pools = [case.pool, case.pool.clone()]          # alternate two caches: each step misses L2
+    if case.q_abs is None:  # fused workload: absorbed queries come from mla_absorb_q first
+        q_abs = mla.absorb_q(case.q_nope, case.q_rope, case.w_uk)
+    else:
+        q_abs = case.q_abs
+    bt = case.block_table.to(dev)
+    sl = case.seq_lens.to(dev)
+    B, Tq = case.B, case.Tq
+    o_lat = torch.empty(B, Tq, 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Tq, 128, dtype=torch.float32, device=dev)
+    ws = torch.empty(mla.decode_workspace_size(B, Tq, 0), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        mla.decode(q_abs, pools[i & 1], bt, sl, case.scale, causal=case.causal, o_lat=o_lat, lse=lse,
+                   workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, word = mla.get_device_status()
+    assert st == 0, f"device status {word:#x}"
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st, word = mla.get_device_status()
+    assert st == 0, f"device status {word:#x}"
+
+    tokens_per_step = B * Tq
+    value = tokens_per_step * args.steps * world / (total_ms / 1000.0)
+    ms_per_step = total_ms / args.steps
+    cache_bytes = int(case.seq_lens.to(torch.int64).sum()) * ROW_BYTES
+    vis = case.seq_lens.to(torch.int64)
+    if case.causal:
+        vis_total = sum(max(0, int(L) - (Tq - 1 - t)) for L in case.seq_lens for t in range(Tq))
+    else:
+        vis_total = int(vis.sum()) * Tq
+    flops = vis_total * FLOP_PER_TOKEN_QUERY
+    avg_launch_s = statistics.mean(per_launch) / 1000.0
+    pk = peaks()
+    achieved_gbs = cache_bytes / avg_launch_s / 1e9
+    achieved_tflops = flops / avg_launch_s / 1e12
+    t_roof = max(cache_bytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    mem_bound = cache_bytes / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_tflops"] * 1e12)
+
+    # end to end through the C ABI with host buffers: queries in, latent output + lse out
+    q_host = q_abs.cpu().pin_memory()
+    o_host = torch.empty(o_lat.shape, dtype=o_lat.dtype).pin_memory()
+    l_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_dev = torch.empty_like(q_abs)
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = o_host.numel() * o_host.element_size() + l_host.numel() * l_host.element_size()
+
+    def e2e_step(i):
+        q_dev.copy_(q_host, non_blocking=True)
+        mla.decode(q_dev, pools[i & 1], bt, sl, case.scale, causal=case.causal, o_lat=o_lat, lse=lse,
+                   workspace=ws, stream=stream)
+        o_host.copy_(o_lat, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_per_step * args.steps * world / (e2e_ms / 1000.0)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if case.q_abs is None:
+            case.q_abs = q_abs
+        rate, cores, sample = cpu_oracle_rate(case, budget_s=12.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        traffic = profiled_traffic(args.workload)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": B, "q_len": Tq, "heads": 128, "d_c": 512, "d_r": 64,
+                       "context": int(case.seq_lens.max()), "total_cached_tokens": int(vis.sum()), "page": 64,
+                       "causal": bool(case.causal), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: two alternating caches of %.0f MB each" % (cache_bytes / 1e6)},
+            "roofline": {"bound": "hbm" if mem_bound else "tensor",
+                         "achieved": achieved_gbs if mem_bound else achieved_tflops,
+                         "peak": pk["hbm_gbs"] if mem_bound else pk["bf16_tflops"],
+                         "unit": "GB/s" if mem_bound else "TFLOP/s",
+                         "frac": (achieved_gbs / pk["hbm_gbs"]) if mem_bound else (achieved_tflops / pk["bf16_tflops"]),
+                         "traffic": traffic,
+                         "peak_source": pk["source"],
+                         "t_roof_us": t_roof * 1e6, "t_launch_us": avg_launch_s * 1e6,
+                         "roofline_frac": t_roof / avg_launch_s,
+                         "tensor_tflops": achieved_tflops, "tensor_frac": achieved_tflops / pk["bf16_tflops"],
+                         "timed_unit": "one mla_decode call (plan + decode + combine kernels)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

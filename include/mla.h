@@ -1,0 +1,164 @@
+/*
+ * mla.h - C ABI of the B300 (sm_103a) Multi-head Latent Attention decode library.
+ *
+ * The method (DeepSeek-V2, as explained on the "DeepSeek-V2" explainer page,
+ * Part B Steps 5-8, and the DeepSeek-V2 paper breakdown, "How It Works"):
+ * every cached token keeps only a 512-number latent c (Step 5, eq. 9) and one
+ * 64-number rotated RoPE key k^R shared by all heads (Step 7), i.e. a
+ * 576-number row per token per layer (Step 8).  The per-head key k = W^UK c
+ * is never built: the query is moved into latent space instead (Step 6,
+ * "absorbing" W^UK), all 128 heads score against the same latent rows, the
+ * content and RoPE scores add inside the softmax (Step 7), and W^UV is
+ * applied to the latent attention output afterwards (Step 6: the values are
+ * never materialised either).
+ *
+ * Fixed shapes: H = 128 heads, d_c = 512 latent, d_r = 64 RoPE, d_h = 128 per
+ * head, row width D = 576, page = 64 tokens.  Element types: bf16 tensors are
+ * passed as `void*` holding IEEE bfloat16 bit patterns; lse is float32.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, 16-byte aligned.  The library allocates no device memory.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work; they return before the GPU has run it.
+ *  - Host-side argument checks happen before anything is enqueued; on a
+ *    failure the call returns the error code and launches nothing.
+ *  - Faults found on the device (a block-table entry outside [0, num_pages),
+ *    a sequence length outside [0, max_pages*64], a wait that timed out) never
+ *    trap: the kernel records a bit in the library's device status word,
+ *    clamps or skips the offending access, and finishes.  Read the word with
+ *    mla_get_device_status().
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so CUDA callers can pass their stream directly. */
+typedef struct CUstream_st *mla_stream_t;
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,   /* null pointer, negative or zero size where one is required */
+    MLA_ERR_SHAPE = 2,         /* sizes outside the supported range */
+    MLA_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+    MLA_ERR_WORKSPACE = 4,     /* workspace null or smaller than mla_decode_workspace_size() */
+    MLA_ERR_UNSUPPORTED = 5,   /* heads != 128, or the current device is not sm_103 */
+    MLA_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed while enqueuing */
+    MLA_ERR_DEVICE_FAULT = 7   /* a device-side guard tripped (see mla_get_device_status) */
+} mla_status_t;
+
+/* Bits of the device status word. */
+#define MLA_DEV_BAD_BLOCK_TABLE 0x1u  /* a block-table entry outside [0, num_pages) was read */
+#define MLA_DEV_BAD_SEQ_LEN     0x2u  /* a sequence length outside [0, max_pages * 64] */
+#define MLA_DEV_WAIT_TIMEOUT    0x4u  /* an on-chip wait gave up (kernel bailed out) */
+#define MLA_DEV_PLAN_OVERFLOW   0x8u  /* the split plan did not fit the workspace */
+
+/*
+ * mla_absorb_q - move the content query into latent space (explainer Step 6,
+ * the 2-d toy example and "absorbing one matrix into another"), and append the
+ * decoupled RoPE query unchanged (Step 7):
+ *     q_abs[n,h,0:512]   = W_UK[h]^T q_nope[n,h,:]      (fp32 accumulate, bf16 out)
+ *     q_abs[n,h,512:576] = q_rope[n,h,:]
+ *
+ * q_nope  [n_tokens, n_heads, 128] bf16
+ * q_rope  [n_tokens, n_heads, 64]  bf16
+ * w_uk    [n_heads, 128, 512]      bf16, W_UK[h] maps a latent c to the key k = W_UK[h] c
+ * q_abs   [n_tokens, n_heads, 576] bf16 (output)
+ * n_heads must be 128; 1 <= n_tokens <= 65536.
+ */
+mla_status_t mla_absorb_q(const void *q_nope, const void *q_rope, const void *w_uk, void *q_abs,
+                          int n_tokens, int n_heads, mla_stream_t stream);
+
+/*
+ * mla_decode_workspace_size - bytes of device workspace mla_decode needs for
+ * this batch.  num_splits is the value that will be passed to mla_decode
+ * (0 = automatic split-KV plan).  Returns 0 for invalid sizes.
+ */
+size_t mla_decode_workspace_size(int batch, int q_len, int num_splits);
+
+/*
+ * mla_decode - weight-absorbed MLA attention over a paged latent cache
+ * (explainer Steps 6-8).  For every sequence b, query token t and head h:
+ *     s_j   = scale * q_abs[b,t,h,:] . row_j          (576-wide: content + RoPE, Step 7)
+ *     o_lat = sum_j softmax(s)_j * row_j[0:512]        (latent output, Step 6)
+ *     lse   = log sum_j exp(s_j)                       (natural log)
+ * over the visible tokens j of sequence b, where row_j =
+ * kv_pool[block_table[b, j / 64], j % 64, :].
+ *
+ * q_abs        [batch, q_len, n_heads, 576] bf16 (from mla_absorb_q, or given)
+ * kv_pool      [num_pages, 64, 576] bf16; row = [c (512) | k^R (64)]
+ * block_table  [batch, max_pages] int32, device; entries past ceil(L_b/64) are not read
+ * seq_lens     [batch] int32, device; L_b = cached tokens of sequence b (never read
+ *              on the host; the q_len new tokens are included when causal)
+ * scale        softmax scale (1/sqrt(192) for DeepSeek-V2 shapes)
+ * causal       0: every query sees all L_b tokens.  1: query t sees tokens
+ *              0 .. L_b - q_len + t (the new tokens are the last q_len rows).
+ * num_splits   0 = automatic split-KV plan from the sequence lengths and SM count;
+ *              k > 0 forces k splits per (sequence, query token) (testing/tuning).
+ * o_lat        [batch, q_len, n_heads, 512] bf16 (output)
+ * lse          [batch, q_len, n_heads] float32 (output); a query with no
+ *              visible token gets o_lat = 0 and lse = -inf.
+ * workspace    device scratch of at least mla_decode_workspace_size() bytes,
+ *              owned by the caller; must not be shared by calls that overlap.
+ * Limits: n_heads == 128; 1 <= batch; 1 <= q_len <= 64; batch * q_len <= 65536;
+ *         max_pages >= 1; num_pages >= 1.
+ */
+mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *block_table,
+                        const int32_t *seq_lens, int batch, int q_len, int n_heads, int num_pages,
+                        int max_pages, float scale, int causal, int num_splits, void *o_lat,
+                        float *lse, void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * mla_combine - merge attention results computed over disjoint token sets
+ * (the split-KV reduction of mla_decode, exposed for callers that split a
+ * sequence themselves, e.g. across devices):
+ *     lse[m] = log sum_r exp(lse_parts[r,m]);  o[m,:] = sum_r exp(lse_parts[r,m] - lse[m]) o_parts[r,m,:]
+ * o_parts [n_parts, rows, 512] float32, lse_parts [n_parts, rows] float32,
+ * o_out [rows, 512] bf16, lse_out [rows] float32.  Parts with lse = -inf
+ * carry no weight; a row whose parts are all -inf gets o = 0, lse = -inf.
+ */
+mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_parts, int rows,
+                         void *o_out, float *lse_out, mla_stream_t stream);
+
+/*
+ * mla_up_proj - regenerate the per-head output from the latent attention output
+ * (explainer Step 5: values v = W^UV c; Step 6: applied after attention):
+ *     out[n,h,:] = W_UV[h] o_lat[n,h,:]          (fp32 accumulate, bf16 out)
+ * o_lat [n_tokens, n_heads, 512] bf16, w_uv [n_heads, 128, 512] bf16,
+ * out [n_tokens, n_heads, 128] bf16.  n_heads must be 128; 1 <= n_tokens <= 65536.
+ */
+mla_status_t mla_up_proj(const void *o_lat, const void *w_uv, void *out, int n_tokens, int n_heads,
+                         mla_stream_t stream);
+
+/*
+ * mla_get_device_status - synchronise `stream`, then read and clear the
+ * library's device status word on the current device (MLA_DEV_* bits).
+ * Returns MLA_ERR_DEVICE_FAULT if any bit was set, MLA_ERR_CUDA if the stream
+ * reported an error, MLA_OK otherwise.  err_word may be NULL.
+ */
+mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t *err_word);
+
+/*
+ * mla_cache_bytes - bytes of latent cache for `tokens` tokens over `layers`
+ * layers: tokens * layers * (d_c + d_r) * bytes_per_elem (explainer Step 8:
+ * 512 + 64 = 576 numbers per token per layer).  Host only.
+ */
+uint64_t mla_cache_bytes(int64_t tokens, int layers, int d_c, int d_r, int bytes_per_elem);
+
+/* Human-readable name of a status code (static string). */
+const char *mla_status_string(mla_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

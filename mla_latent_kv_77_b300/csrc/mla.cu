@@ -1,0 +1,346 @@
+// mla.cu - C ABI of the MLA decode library (declared in include/mla.h).
+// Host side only: argument checks, TMA descriptors, launch configuration.
+// Every numeric step runs in the kernels of decode_kernels.cuh / gemm_kernels.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "../../include/mla_testing.h"
+#include "decode_kernels.cuh"
+#include "gemm_kernels.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxClusters = 160;     // workspace is sized for at most this many CTA pairs
+constexpr int kMaxRows = 65536;       // batch * q_len limit of the planner
+constexpr int kMaxQLen = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sms = 0;
+    int clusters = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Per-device setup, once: capability check, kernel attributes, co-resident CTA pairs.
+mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MLA_ERR_CUDA;
+        d.supported = (prop.major == 10 && prop.minor == 3);
+        d.sms = prop.multiProcessorCount;
+        if (d.supported) {
+            if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmem) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
+                    cudaSuccess)
+                return MLA_ERR_CUDA;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
+            cfg.blockDim = dim3(192, 1, 1);
+            cfg.dynamicSmemBytes = kDecodeSmem;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int nc = 0;
+            if (cudaOccupancyMaxActiveClusters(&nc, (const void *)decode_kernel, &cfg) != cudaSuccess || nc <= 0) {
+                cudaGetLastError();
+                nc = d.sms / 2;
+            }
+            d.clusters = nc < kMaxClusters ? nc : kMaxClusters;
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return MLA_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return MLA_ERR_UNSUPPORTED;
+    *dev_out = dev;
+    *info_out = &d;
+    return MLA_OK;
+}
+
+// 2-D bf16 tensor map: `rows` rows of `cols` elements, `row_bytes` apart; boxes of
+// box_cols x box_rows with 128-byte swizzle (box_cols * 2 must be 128).
+bool tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+             uint32_t box_rows) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t hdr, items, info, part_lse, part_o, total;
+    int max_items, max_slots;
+};
+
+bool ws_layout(int batch, int q_len, int num_splits, WsLayout *w) {
+    if (batch < 1 || q_len < 1 || q_len > kMaxQLen || num_splits < 0 || num_splits > 4096) return false;
+    const long long n_bt = (long long)batch * q_len;
+    if (n_bt > kMaxRows) return false;
+    long long mi = num_splits > 0 ? n_bt * num_splits : n_bt + kMaxClusters;
+    if (mi > (1ll << 24)) return false;
+    w->max_items = (int)mi;
+    w->max_slots = (int)mi;
+    size_t off = 0;
+    w->hdr = off;
+    off = align_up(off + sizeof(PlanHeader), 256);
+    w->items = off;
+    off = align_up(off + sizeof(Item) * (size_t)mi, 256);
+    w->info = off;
+    off = align_up(off + sizeof(BtInfo) * (size_t)n_bt, 256);
+    w->part_lse = off;
+    off = align_up(off + sizeof(float) * kHeads * (size_t)mi, 256);
+    w->part_o = off;
+    off = align_up(off + sizeof(float) * kHeads * kDc * (size_t)mi, 256);
+    w->total = off;
+    return true;
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait gives up.
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        mbar_wait(smem_u32(&bar), 0u, &abort_flag, limit_ns);
+    }
+}
+
+mla_status_t launch_error() {
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char *mla_status_string(mla_status_t s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+        case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE";
+        case MLA_ERR_ALIGNMENT: return "MLA_ERR_ALIGNMENT";
+        case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+        case MLA_ERR_DEVICE_FAULT: return "MLA_ERR_DEVICE_FAULT";
+    }
+    return "MLA_ERR_UNKNOWN";
+}
+
+uint64_t mla_cache_bytes(int64_t tokens, int layers, int d_c, int d_r, int bytes_per_elem) {
+    if (tokens < 0 || layers < 0 || d_c < 0 || d_r < 0 || bytes_per_elem < 0) return 0;
+    return (uint64_t)tokens * (uint64_t)layers * (uint64_t)(d_c + d_r) * (uint64_t)bytes_per_elem;
+}
+
+size_t mla_decode_workspace_size(int batch, int q_len, int num_splits) {
+    WsLayout w;
+    if (!ws_layout(batch, q_len, num_splits, &w)) return 0;
+    return w.total;
+}
+
+mla_status_t mla_absorb_q(const void *q_nope, const void *q_rope, const void *w_uk, void *q_abs, int n_tokens,
+                          int n_heads, mla_stream_t stream) {
+    if (!q_nope || !q_rope || !w_uk || !q_abs) return MLA_ERR_INVALID_ARG;
+    if (n_tokens < 1) return MLA_ERR_INVALID_ARG;
+    if (n_heads != kHeads) return MLA_ERR_UNSUPPORTED;
+    if (n_tokens > kMaxRows) return MLA_ERR_SHAPE;
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    CUtensorMap tw, tx;
+    if (!tmap_2d(&tw, w_uk, kDc, (uint64_t)kHeads * 128, kDc * 2, 64, 64)) return MLA_ERR_CUDA;
+    if (!tmap_2d(&tx, q_nope, (uint64_t)kHeads * 128, (uint64_t)n_tokens, (uint64_t)kHeads * 128 * 2, 64, 128))
+        return MLA_ERR_CUDA;
+    GemmParams p;
+    p.mode = kModeAbsorb;
+    p.n_tokens = n_tokens;
+    p.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
+    p.out = static_cast<__nv_bfloat16 *>(q_abs);
+    dim3 grid(kHeads, kDc / 128, (n_tokens + kGemmTileN - 1) / kGemmTileN);
+    head_gemm_kernel<<<grid, 192, kGemmSmem, (cudaStream_t)stream>>>(tw, tx, p);
+    return launch_error();
+}
+
+mla_status_t mla_up_proj(const void *o_lat, const void *w_uv, void *out, int n_tokens, int n_heads,
+                         mla_stream_t stream) {
+    if (!o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    if (n_tokens < 1) return MLA_ERR_INVALID_ARG;
+    if (n_heads != kHeads) return MLA_ERR_UNSUPPORTED;
+    if (n_tokens > kMaxRows) return MLA_ERR_SHAPE;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    CUtensorMap tw, tx;
+    if (!tmap_2d(&tw, w_uv, kDc, (uint64_t)kHeads * 128, kDc * 2, 64, 128)) return MLA_ERR_CUDA;
+    if (!tmap_2d(&tx, o_lat, (uint64_t)kHeads * kDc, (uint64_t)n_tokens, (uint64_t)kHeads * kDc * 2, 64, 128))
+        return MLA_ERR_CUDA;
+    GemmParams p;
+    p.mode = kModeUpProj;
+    p.n_tokens = n_tokens;
+    p.q_rope = nullptr;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    dim3 grid(kHeads, 1, (n_tokens + kGemmTileN - 1) / kGemmTileN);
+    head_gemm_kernel<<<grid, 192, kGemmSmem, (cudaStream_t)stream>>>(tw, tx, p);
+    return launch_error();
+}
+
+mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *block_table, const int32_t *seq_lens,
+                        int batch, int q_len, int n_heads, int num_pages, int max_pages, float scale, int causal,
+                        int num_splits, void *o_lat, float *lse, void *workspace, size_t workspace_bytes,
+                        mla_stream_t stream) {
+    if (!q_abs || !kv_pool || !block_table || !seq_lens || !o_lat || !lse) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || q_len < 1 || num_pages < 1 || max_pages < 1 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+    if (n_heads != kHeads) return MLA_ERR_UNSUPPORTED;
+    if (q_len > kMaxQLen || (long long)batch * q_len > kMaxRows) return MLA_ERR_SHAPE;
+    if ((long long)num_pages * kPage > 0x7fffffffll || (long long)max_pages * kPage > 0x7fffffffll) return MLA_ERR_SHAPE;
+    if (!aligned16(q_abs) || !aligned16(kv_pool) || !aligned16(o_lat) || !aligned4(lse) || !aligned4(block_table) ||
+        !aligned4(seq_lens))
+        return MLA_ERR_ALIGNMENT;
+    WsLayout w;
+    if (!ws_layout(batch, q_len, num_splits, &w)) return MLA_ERR_SHAPE;
+    if (!workspace || workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+
+    CUtensorMap tkv;
+    if (!tmap_2d(&tkv, kv_pool, kD, (uint64_t)num_pages * kPage, kD * 2, 64, kPage)) return MLA_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + w.hdr);
+    Item *items = reinterpret_cast<Item *>(ws + w.items);
+    BtInfo *bt_info = reinterpret_cast<BtInfo *>(ws + w.info);
+    const int n_bt = batch * q_len;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    plan_kernel<<<1, kPlanThreads, 0, s>>>(seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
+                                           num_splits, hdr, items, bt_info, w.max_items, w.max_slots);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+    DecodeParams p;
+    p.q_abs = static_cast<const __nv_bfloat16 *>(q_abs);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.o_lat = static_cast<__nv_bfloat16 *>(o_lat);
+    p.lse = lse;
+    p.hdr = hdr;
+    p.items = items;
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+    p.B = batch;
+    p.Tq = q_len;
+    p.causal = causal ? 1 : 0;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.sl2 = scale * 1.4426950408889634f;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * info->clusters, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = kDecodeSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel, tkv, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    combine_kernel<<<dim3(n_bt, kHeads / 8), 128, 0, s>>>(bt_info, p.part_o, p.part_lse, p.o_lat, lse);
+    return launch_error();
+}
+
+mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_parts, int rows, void *o_out,
+                         float *lse_out, mla_stream_t stream) {
+    if (!o_parts || !lse_parts || !o_out || !lse_out) return MLA_ERR_INVALID_ARG;
+    if (n_parts < 1 || rows < 1) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_parts) || !aligned4(lse_parts) || !aligned16(o_out) || !aligned4(lse_out))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    combine_rows_kernel<<<(rows + 7) / 8, 128, 0, (cudaStream_t)stream>>>(
+        o_parts, lse_parts, n_parts, rows, static_cast<__nv_bfloat16 *>(o_out), lse_out);
+    return launch_error();
+}
+
+mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream) {
+    if (limit_ms < 1 || limit_ms > 10000) return MLA_ERR_INVALID_ARG;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    bounded_wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ms * 1000000ull);
+    return launch_error();
+}
+
+mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t *err_word) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
+    uint32_t v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(z)) != cudaSuccess) return MLA_ERR_CUDA;
+    if (err_word) *err_word = v;
+    return v ? MLA_ERR_DEVICE_FAULT : MLA_OK;
+}
+
+}  // extern "C"

@@ -126,7 +126,10 @@ def decode_absorbed(q_abs, pool, block_table, seq_lens, scale: float, causal: bo
     """
     pl = _f32(pool)
     bt, sl = _i32(block_table), _i32(seq_lens)
-    if hasattr(q_abs, "detach") or np.asarray(q_abs).dtype != np.float64:
+    if hasattr(q_abs, "detach"):
+        q_abs = q_abs.detach().to("cpu")
+        q_abs = q_abs.double().numpy() if str(q_abs.dtype) == "torch.float64" else q_abs.float().numpy()
+    if np.asarray(q_abs).dtype != np.float64:
         q32, q64 = _f32(q_abs), None
         q = q32
     else:

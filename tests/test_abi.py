@@ -1,0 +1,126 @@
+"""The C-ABI library loads, exports every function include/*.h declares, and rejects
+bad arguments on the host (no GPU needed: these calls return before any CUDA call)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_77_b300 as mla
+from mla_latent_kv_77_b300 import build as mla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "mla_decode" in declared and "mla_absorb_q" in declared and "mla_up_proj" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(mla.EXPORTS), (set(declared) ^ set(mla.EXPORTS))
+
+
+def test_version_and_status_strings(lib):
+    assert mla.version() >= 100
+    for s in mla.Status:
+        assert mla.status_string(int(s)) == "MLA_" + ("OK" if s == 0 else "ERR_" + s.name)
+
+
+def test_cache_bytes_matches_printed_arithmetic(lib):
+    """Step 8: 576 numbers per token per layer; 128K tokens x 60 layers x 2 bytes ~ 9.1 GB."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "cache_arithmetic.json")))
+    pr = g["printed"]
+    per_token = mla.cache_bytes(1, 60, 512, 64, 1)
+    assert per_token == pr["mla_numbers_per_token"]["value"]
+    assert mla.cache_bytes(1, 1, 512, 64, 1) == pr["mla_numbers_per_token_layer"]["value"]
+    gb = mla.cache_bytes(131072, 60, 512, 64, 2) / 1e9
+    assert abs(gb - pr["mla_gb_report"]["value"]) <= pr["mla_gb_report"]["rounding"]
+    assert mla.cache_bytes(-1, 60, 512, 64, 2) == 0
+
+
+def test_workspace_size(lib):
+    a = mla.decode_workspace_size(64, 1, 0)
+    assert a > 0
+    assert mla.decode_workspace_size(64, 1, 4) > 0
+    assert mla.decode_workspace_size(0, 1, 0) == 0
+    assert mla.decode_workspace_size(1, 65, 0) == 0        # q_len above the limit
+    assert mla.decode_workspace_size(65536, 2, 0) == 0     # too many rows
+    assert mla.decode_workspace_size(128, 1, 0) > mla.decode_workspace_size(64, 1, 0)
+
+
+def _decode_args(**over):
+    ws_bytes = mla.decode_workspace_size(2, 1, 0)
+    a = dict(q=16, kv=32, bt=48, sl=64, B=2, Tq=1, H=128, P=4, maxp=2, scale=0.07, causal=0, splits=0,
+             o=80, lse=96, ws=128, ws_bytes=ws_bytes, stream=None)
+    a.update(over)
+    return a
+
+
+def _call_decode(lib, a):
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    return lib.mla_decode(vp(a["q"]), vp(a["kv"]), vp(a["bt"]), vp(a["sl"]), a["B"], a["Tq"], a["H"], a["P"],
+                          a["maxp"], a["scale"], a["causal"], a["splits"], vp(a["o"]), vp(a["lse"]), vp(a["ws"]),
+                          a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), mla.Status.INVALID_ARG),
+    (dict(kv=None), mla.Status.INVALID_ARG),
+    (dict(bt=None), mla.Status.INVALID_ARG),
+    (dict(sl=None), mla.Status.INVALID_ARG),
+    (dict(o=None), mla.Status.INVALID_ARG),
+    (dict(lse=None), mla.Status.INVALID_ARG),
+    (dict(B=0), mla.Status.INVALID_ARG),
+    (dict(Tq=0), mla.Status.INVALID_ARG),
+    (dict(P=0), mla.Status.INVALID_ARG),
+    (dict(splits=-1), mla.Status.INVALID_ARG),
+    (dict(scale=0.0), mla.Status.INVALID_ARG),
+    (dict(scale=float("nan")), mla.Status.INVALID_ARG),
+    (dict(H=64), mla.Status.UNSUPPORTED),
+    (dict(Tq=65), mla.Status.SHAPE),
+    (dict(q=24), mla.Status.ALIGNMENT),
+    (dict(kv=8), mla.Status.ALIGNMENT),
+    (dict(ws=None), mla.Status.WORKSPACE),
+    (dict(ws_bytes=100), mla.Status.WORKSPACE),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, over, code):
+    assert _call_decode(lib, _decode_args(**over)) == code
+
+
+def test_absorb_and_up_proj_reject_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+    assert lib.mla_absorb_q(None, vp(16), vp(32), vp(48), 4, 128, None) == mla.Status.INVALID_ARG
+    assert lib.mla_absorb_q(vp(16), vp(16), vp(32), vp(48), 0, 128, None) == mla.Status.INVALID_ARG
+    assert lib.mla_absorb_q(vp(16), vp(16), vp(32), vp(48), 4, 96, None) == mla.Status.UNSUPPORTED
+    assert lib.mla_absorb_q(vp(18), vp(16), vp(32), vp(48), 4, 128, None) == mla.Status.ALIGNMENT
+    assert lib.mla_up_proj(vp(16), None, vp(48), 4, 128, None) == mla.Status.INVALID_ARG
+    assert lib.mla_up_proj(vp(16), vp(32), vp(48), 4, 100, None) == mla.Status.UNSUPPORTED
+    assert lib.mla_up_proj(vp(16), vp(32), vp(50), 4, 128, None) == mla.Status.ALIGNMENT
+    assert lib.mla_combine(None, vp(16), 2, 4, vp(32), vp(48), None) == mla.Status.INVALID_ARG
+    assert lib.mla_combine(vp(16), vp(16), 0, 4, vp(32), vp(48), None) == mla.Status.INVALID_ARG
+    assert lib.mla_test_bounded_wait(0, None) == mla.Status.INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(mla, "_lib", None)
+    monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(mla.MLAError):
+        mla.lib()
