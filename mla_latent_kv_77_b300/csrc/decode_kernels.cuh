@@ -442,7 +442,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
                 float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
                 pk[c] = pack_bf16x2(a, b);
-                lsum += bf16lo_to_f32(pk[c]) + bf16hi_to_f32(pk[c]);
+                lsum += a + b;  // the row sum uses the unrounded probabilities (exact lse)
             }
             l += lsum;
 
