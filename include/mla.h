@@ -114,6 +114,40 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
                         int max_pages, float scale, int causal, int num_splits, void *o_lat,
                         float *lse, void *workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/* Size of the library-owned scratch used by mla_decode_static_scratch (64 MiB). */
+#define MLA_STATIC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * mla_decode_static_scratch - mla_decode for callers that cannot allocate device
+ * memory.  The paper has no counterpart to this call; it exists for integration only.
+ *
+ * Some callers have no way to obtain device memory: a plug-in running inside a host
+ * application that owns every device allocation and hands plug-ins no allocator, or a
+ * serving loop whose rule is "no cudaMalloc after start-up" because an allocation can
+ * synchronise the device and stall the requests in flight.  This call takes the same
+ * arguments as mla_decode minus the workspace, and uses instead a fixed scratch array
+ * of MLA_STATIC_SCRATCH_BYTES that the library keeps in device memory.  Every GPU that
+ * loads the library holds that array until the process exits.  The call allocates
+ * nothing itself.
+ *
+ * Limit: requests whose mla_decode_workspace_size(batch, q_len, num_splits) exceeds
+ * MLA_STATIC_SCRATCH_BYTES are rejected with MLA_ERR_WORKSPACE before anything is
+ * enqueued.  With the automatic plan (num_splits = 0) that admits batch * q_len up to 95.
+ *
+ * First call per device: it looks up the device address of the array (with that
+ * device current), once; make that first call before any stream capture begins.
+ *
+ * Sharing: all calls on a device use the same array, which keeps whatever the previous
+ * call left there.  Nothing in it needs to start at zero (the planning kernel rewrites
+ * every field the later kernels read), but calls whose GPU execution overlaps -- two
+ * streams, or two host threads on one device -- race on the array and corrupt each
+ * other's results.  Keep them ordered: one stream, or synchronise between them.
+ */
+mla_status_t mla_decode_static_scratch(const void *q_abs, const void *kv_pool, const int32_t *block_table,
+                                       const int32_t *seq_lens, int batch, int q_len, int n_heads,
+                                       int num_pages, int max_pages, float scale, int causal, int num_splits,
+                                       void *o_lat, float *lse, mla_stream_t stream);
+
 /*
  * mla_combine - merge attention results computed over disjoint token sets
  * (the split-KV reduction of mla_decode, exposed for callers that split a

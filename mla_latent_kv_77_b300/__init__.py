@@ -61,6 +61,7 @@ EXPORTS = {
     "mla_absorb_q": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP]),
     "mla_decode_workspace_size": (_SZ, [_I, _I, _I]),
     "mla_decode": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _VP, _VP, _SZ, _VP]),
+    "mla_decode_static_scratch": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _VP, _VP]),
     "mla_combine": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP]),
     "mla_up_proj": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "mla_get_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
@@ -181,6 +182,28 @@ def decode(q_abs, kv_pool, block_table, seq_lens, scale: float = SCALE, causal: 
                           int(num_splits), _ptr(o_lat), _ptr(lse), _ptr(workspace), workspace.numel(),
                           _stream(stream))
     _check(st, "mla_decode")
+    return o_lat, lse
+
+
+def decode_static_scratch(q_abs, kv_pool, block_table, seq_lens, scale: float = SCALE, causal: bool = False,
+                          num_splits: int = 0, o_lat=None, lse=None, stream=None) -> Tuple:
+    """Like decode(), without a workspace: the library's own fixed device scratch is used
+    (for callers that cannot allocate; calls on one device must not overlap)."""
+    import torch
+    _need(q_abs, torch.bfloat16, "q_abs")
+    _need(kv_pool, torch.bfloat16, "kv_pool")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Tq, nh, _ = q_abs.shape
+    if o_lat is None:
+        o_lat = torch.empty(B, Tq, nh, D_C, dtype=torch.bfloat16, device=q_abs.device)
+    if lse is None:
+        lse = torch.empty(B, Tq, nh, dtype=torch.float32, device=q_abs.device)
+    st = lib().mla_decode_static_scratch(_ptr(q_abs), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), B, Tq,
+                                         nh, kv_pool.shape[0], block_table.shape[1], float(scale),
+                                         int(bool(causal)), int(num_splits), _ptr(o_lat), _ptr(lse),
+                                         _stream(stream))
+    _check(st, "mla_decode_static_scratch")
     return o_lat, lse
 
 

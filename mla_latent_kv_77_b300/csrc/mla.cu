@@ -152,7 +152,17 @@ mla_status_t launch_error() {
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// Device address of the library-owned decode scratch on each device, looked up once.
+void *g_scratch_addr[kMaxDevices] = {};
+
 }  // namespace
+
+// Scratch for mla_decode_static_scratch: lives in the library's own device memory, so
+// that entry point never allocates.  Every device that loads the library holds it until
+// the process exits.  Host code must not pass this name to a kernel: on the host it is
+// only a stand-in; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_decode_scratch[MLA_STATIC_SCRATCH_BYTES];
+
 }  // namespace mla
 
 using namespace mla;
@@ -307,6 +317,36 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     }
     combine_kernel<<<dim3(n_bt, kHeads / 8), 128, 0, s>>>(bt_info, p.part_o, p.part_lse, p.o_lat, lse);
     return launch_error();
+}
+
+mla_status_t mla_decode_static_scratch(const void *q_abs, const void *kv_pool, const int32_t *block_table,
+                                       const int32_t *seq_lens, int batch, int q_len, int n_heads, int num_pages,
+                                       int max_pages, float scale, int causal, int num_splits, void *o_lat,
+                                       float *lse, mla_stream_t stream) {
+    const size_t need = mla_decode_workspace_size(batch, q_len, num_splits);
+    if (need == 0)  // sizes mla_decode itself rejects: let it report the reason
+        return mla_decode(q_abs, kv_pool, block_table, seq_lens, batch, q_len, n_heads, num_pages, max_pages,
+                          scale, causal, num_splits, o_lat, lse, nullptr, 0, stream);
+    if (need > (size_t)MLA_STATIC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_scratch_addr[dev] == nullptr) {
+            // first call on this device (which is current): find where the array lives
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_decode_scratch) != cudaSuccess || addr == nullptr) {
+                cudaGetLastError();
+                return MLA_ERR_CUDA;
+            }
+            g_scratch_addr[dev] = addr;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    return mla_decode(q_abs, kv_pool, block_table, seq_lens, batch, q_len, n_heads, num_pages, max_pages, scale,
+                      causal, num_splits, o_lat, lse, scratch, (size_t)MLA_STATIC_SCRATCH_BYTES, stream);
 }
 
 mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_parts, int rows, void *o_out,
