@@ -34,10 +34,13 @@ constexpr int kDc = 512;
 constexpr int kDr = 64;
 constexpr int kD = kDc + kDr;        // 576
 constexpr int kPage = 64;            // tokens per page == tokens per tile
-constexpr int kBoxBytes = kPage * 128;  // 64 rows x 64 bf16
-constexpr int kBoxesS = kD / 64;     // 9 boxes per page for scoring
-constexpr int kBoxesV = kDc / 64;    // 8 boxes per page for the value side
-constexpr int kRing = 20;            // ring slots (a multiple of 4: half-pages never wrap)
+constexpr int kBoxBytes = kPage * 128;  // one 64-row x 64-column bf16 block (128-byte rows)
+constexpr int kBoxesS = kD / 64;     // 9 blocks per page for scoring (c and k^R)
+constexpr int kBoxesV = kDc / 64;    // 8 blocks per page for the value side (c only)
+constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page
+constexpr uint32_t kStageV = kBoxesV * kBoxBytes;  // 65536: a page's latent columns
+constexpr int kStages = 2;           // page stages per CTA
+constexpr int kPBufs = 4;            // P messages in flight between the two CTAs
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1040;     // alpha[128] f32, inv_l[128] f32, flags, valid, pad
 constexpr int kMetaStride = 1088;
@@ -48,32 +51,35 @@ constexpr uint32_t kTmemS = 0;       // score CTA: S buffers at 0 and 64
 constexpr uint32_t kTmemQ = 128;     // score CTA: Q (bf16 pairs) at 128 .. 415
 constexpr uint32_t kTmemCols = 512;
 
-// shared memory layout (identical in both CTAs, offsets from a 1024-aligned base)
-constexpr uint32_t kOffRing = 0;
-constexpr uint32_t kOffP = kOffRing + kRing * kBoxBytes;           // 163840
-constexpr uint32_t kOffMeta = kOffP + 2 * kPBytes;                  // 196608
-constexpr uint32_t kOffBar = kOffMeta + 2 * kMetaStride;            // 198784
+// Shared memory (offsets from a 1024-aligned base).  The message area and the barriers sit
+// at the same offsets in both CTAs (the partner addresses them remotely); the page stages
+// follow, 72 KB each in the score CTA and 64 KB each in the accumulate CTA.
+constexpr uint32_t kOffP = 0;                                       // kPBufs x 16 KB
+constexpr uint32_t kOffMeta = kOffP + kPBufs * kPBytes;             // kPBufs x 1088
+constexpr uint32_t kOffEvt = kOffMeta + kPBufs * kMetaStride;       // alpha[128], inv_l[128], type
+constexpr uint32_t kOffBar = kOffEvt + 1040;
 constexpr int kBarFull = 0;
-constexpr int kBarEmpty = kBarFull + kRing;
-constexpr int kBarSFull = kBarEmpty + kRing;
+constexpr int kBarEmpty = kBarFull + kStages;
+constexpr int kBarSFull = kBarEmpty + kStages;
 constexpr int kBarSEmpty = kBarSFull + 2;
 constexpr int kBarQReady = kBarSEmpty + 2;
 constexpr int kBarPFree = kBarQReady + 1;
-constexpr int kBarPFull = kBarPFree + 2;
-constexpr int kBarMmaEvt = kBarPFull + 2;
+constexpr int kBarPFull = kBarPFree + kPBufs;
+constexpr int kBarPStaged = kBarPFull + kPBufs;
+constexpr int kBarMmaEvt = kBarPStaged + kPBufs;
 constexpr int kBarCorrEvt = kBarMmaEvt + 1;
-constexpr int kBarPStaged = kBarCorrEvt + 1;
-constexpr int kNumBars = kBarPStaged + 2;
+constexpr int kNumBars = kBarCorrEvt + 1;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kOffAny = kOffAbort + 4;   // two words: OR of the rescale requests per P buffer
-constexpr uint32_t kSmemUsed = kOffAny + 8;
-constexpr uint32_t kDecodeSmem = kSmemUsed + 1024;  // slack for aligning the base
+constexpr uint32_t kOffAny = kOffAbort + 4;  // kPBufs words: OR of the rescale requests per message
+constexpr uint32_t kOffStages = (kOffAny + 4 * kPBufs + 1023u) & ~1023u;
+constexpr uint32_t kDecodeSmem = kOffStages + kStages * kStageS + 1024;  // + slack to align the base
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);    // A = Q (TMEM), B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A = P K-major, B = V MN-major
 
 constexpr uint32_t kFlagFirst = 1u, kFlagRescale = 2u, kFlagLast = 4u;
+constexpr uint32_t kEvtRescale = 1u, kEvtEpilogue = 2u;
 
 // One unit of work: tiles [tb, te) of query (b, t) where bt = b * Tq + t.
 // slot < 0: the item covers the whole query and writes the final output;
@@ -292,43 +298,53 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
 struct Smem {
     uint32_t base;  // shared::cta address of the aligned base
     __device__ __forceinline__ uint32_t bar(int i) const { return base + kOffBar + 8u * i; }
-    __device__ __forceinline__ uint32_t ring(uint32_t slot) const { return base + kOffRing + slot * kBoxBytes; }
+    __device__ __forceinline__ uint32_t stage(uint32_t s, uint32_t bytes) const { return base + kOffStages + s * bytes; }
     __device__ __forceinline__ uint32_t pbuf(uint32_t j) const { return base + kOffP + j * kPBytes; }
     __device__ __forceinline__ uint32_t meta(uint32_t j) const { return base + kOffMeta + j * kMetaStride; }
+    __device__ __forceinline__ uint32_t evt() const { return base + kOffEvt; }
 };
 
-// Producer: TMA loads of each item's pages, `nbox` 64-column boxes per page.
+__device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Producer: one TMA per page.  The tensor map views the pool as (64 columns, rows, column
+// blocks) with strides (2 B, 1152 B, 128 B), so a single box lands in shared memory as
+// `blocks` consecutive 64-row x 128-byte swizzled blocks -- the operand layout of the MMAs.
 __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                              int nbox, int cid, int ncl, int n_items,
+                                              uint32_t stage_bytes, int cid, int ncl, int n_items,
                                               volatile int *abort) {
     uint32_t g = 0;
     for (int r = 0;; ++r) {
         int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
         ItemInfo it = load_item(p, i);
-        for (int tile = it.tb; tile < it.te; ++tile) {
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             int pg = p.block_table[(size_t)it.b * p.max_pages + tile];
             if (pg < 0 || pg >= p.num_pages) {
                 raise_status(0x1u);
                 pg = 0;
             }
-            for (int bx = 0; bx < nbox; ++bx, ++g) {
-                uint32_t s = g % kRing;
-                if (!mbar_wait(sm.bar(kBarEmpty + s), ((g / kRing) & 1u) ^ 1u, abort)) return;
-                mbar_arrive_expect_tx(sm.bar(kBarFull + s), kBoxBytes);
-                tma_load_2d(sm.ring(s), tmap, bx * 64, pg * kPage, sm.bar(kBarFull + s));
-            }
+            const uint32_t s = g % kStages;
+            if (!mbar_wait(sm.bar(kBarEmpty + s), ((g / kStages) & 1u) ^ 1u, abort)) return;
+            mbar_arrive_expect_tx(sm.bar(kBarFull + s), stage_bytes);
+            tma_load_3d(sm.stage(s, stage_bytes), tmap, 0, pg * kPage, 0, sm.bar(kBarFull + s));
         }
     }
     // let every load issued land before the CTA can retire (bounded)
-    for (uint32_t k = (g > kRing ? g - kRing : 0); k < g; ++k)
-        if (!mbar_wait(sm.bar(kBarFull + k % kRing), (k / kRing) & 1u, abort)) return;
+    for (uint32_t k = (g > kStages ? g - kStages : 0); k < g; ++k)
+        if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
 }
 
 // Score CTA, MMA issuer (one thread): S_j = Q . K_tile^T, K = 576 in 36 steps.
 __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
                                                int ncl, int n_items, volatile int *abort) {
-    uint32_t g = 0, sc = 0, ic = 0;
+    uint32_t g = 0, ic = 0;
     for (int r = 0;; ++r) {
         int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
@@ -337,23 +353,22 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
         if (!mbar_wait(sm.bar(kBarQReady), ic & 1u, abort)) return;
         tc_fence_after();
         ++ic;
-        for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
-            uint32_t j = sc & 1u;
-            if (!mbar_wait(sm.bar(kBarSEmpty + j), ((sc >> 1) & 1u) ^ 1u, abort)) return;
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            const uint32_t j = g & 1u, s = g % kStages;
+            if (!mbar_wait(sm.bar(kBarSEmpty + j), ((g >> 1) & 1u) ^ 1u, abort)) return;
+            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStages) & 1u, abort)) return;
             tc_fence_after();
             const uint32_t d = tmem + kTmemS + j * 64u;
-            for (int bx = 0; bx < kBoxesS; ++bx, ++g) {
-                uint32_t s = g % kRing;
-                if (!mbar_wait(sm.bar(kBarFull + s), (g / kRing) & 1u, abort)) return;
-                tc_fence_after();
-                const uint32_t kb = sm.ring(s);
+            const uint32_t kb = sm.stage(s, kStageS);
+#pragma unroll 1
+            for (int bx = 0; bx < kBoxesS; ++bx) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    uint64_t bdesc = sdesc_sw128(kb + 32u * k, 16u, 1024u);
+                    uint64_t bdesc = sdesc_sw128(kb + bx * kBoxBytes + 32u * k, 16u, 1024u);
                     mma_ts(d, tmem + kTmemQ + bx * 32u + k * 8u, bdesc, kIdescS, (bx | k) != 0);
                 }
-                mma_commit(sm.bar(kBarEmpty + s));
             }
+            mma_commit(sm.bar(kBarEmpty + s));
             mma_commit(sm.bar(kBarSFull + j));
         }
     }
@@ -366,9 +381,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
     const int h = threadIdx.x;  // 0..127
     const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
     const float sl2 = p.sl2;
-    uint32_t sc = 0, pc = 0;
-    const uint32_t peer_bar_full[2] = {mapa_shared(sm.bar(kBarPFull + 0), 1),
-                                       mapa_shared(sm.bar(kBarPFull + 1), 1)};
+    uint32_t sc = 0;
     for (int r = 0;; ++r) {
         int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
@@ -398,7 +411,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             mbar_arrive(sm.bar(kBarQReady));
         }
         float m = 0.f, l = 0.f;
-        for (int tile = it.tb; tile < it.te; ++tile, ++sc, ++pc) {
+        for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
             const uint32_t j = sc & 1u;
             if (!mbar_wait(sm.bar(kBarSFull + j), (sc >> 1) & 1u, abort)) return;
             tc_fence_after();
@@ -447,8 +460,8 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             l += lsum;
 
             // ship P, alpha (and 1/l on the last tile) to the accumulate CTA
-            const uint32_t jp = pc & 1u;
-            if (!mbar_wait<true>(sm.bar(kBarPFree + jp), ((pc >> 1) & 1u) ^ 1u, abort)) return;
+            const uint32_t jp = sc % kPBufs, use = sc / kPBufs;
+            if (!mbar_wait<true>(sm.bar(kBarPFree + jp), (use & 1u) ^ 1u, abort)) return;
             {
                 const uint32_t row = sm.pbuf(jp) + (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u;
 #pragma unroll
@@ -468,7 +481,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             mbar_arrive(sm.bar(kBarPStaged + jp));
             if (h == 0) {
                 // all 128 rows staged: send the message (bounded wait, no hardware barrier)
-                if (!mbar_wait(sm.bar(kBarPStaged + jp), (pc >> 1) & 1u, abort)) return;
+                if (!mbar_wait(sm.bar(kBarPStaged + jp), use & 1u, abort)) return;
                 const uint32_t any = any_words[jp];
                 any_words[jp] = 0u;
                 const uint32_t flags = (first ? kFlagFirst : 0u) | (any ? kFlagRescale : 0u) | (last ? kFlagLast : 0u);
@@ -476,8 +489,9 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mt + 1024u), "r"(flags), "r"((uint32_t)valid)
                              : "memory");
                 fence_proxy_async_smem();
-                bulk_copy_s2c(mapa_shared(sm.pbuf(jp), 1), sm.pbuf(jp), kPBytes, peer_bar_full[jp]);
-                bulk_copy_s2c(mapa_shared(mt, 1), mt, kMetaBytes, peer_bar_full[jp]);
+                const uint32_t peer_full = mapa_shared(sm.bar(kBarPFull + jp), 1);
+                bulk_copy_s2c(mapa_shared(sm.pbuf(jp), 1), sm.pbuf(jp), kPBytes, peer_full);
+                bulk_copy_s2c(mapa_shared(mt, 1), mt, kMetaBytes, peer_full);
             }
         }
         const float lse = (m + __log2f(l)) * 0.69314718055994531f;
@@ -488,24 +502,28 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
     }
 }
 
-// Accumulate CTA, MMA warp: O += P V, two N = 256 halves, K = 64 in 4 steps.
+// Accumulate CTA, MMA warp: O += P V, two N = 256 halves, K = 64 in 4 steps.  It also
+// hands rescale and epilogue events to the epilogue warps through the local event buffer:
+// the event data is written, then the event barrier gets two arrivals -- this warp's
+// (release: the data is visible) and the MMA commit (all earlier MMAs have completed).
 __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
                                                int ncl, int n_items, volatile int *abort) {
     const int lane = threadIdx.x & 31;
-    uint32_t g = 0, pc = 0, cv = 0;
+    uint32_t g = 0, cv = 0;
     bool pending_epilogue = false;
+    const uint32_t evt = sm.evt();
     for (int r = 0;; ++r) {
         int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
         ItemInfo it = load_item(p, i);
-        for (int tile = it.tb; tile < it.te; ++tile, ++pc, g += kBoxesV) {
-            const uint32_t jp = pc & 1u;
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            const uint32_t jp = g % kPBufs, use = g / kPBufs, s = g % kStages;
             if (lane == 0) mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kPBytes + kMetaBytes);
             __syncwarp();
-            if (!mbar_wait<true>(sm.bar(kBarPFull + jp), (pc >> 1) & 1u, abort)) return;
+            if (!mbar_wait<true>(sm.bar(kBarPFull + jp), use & 1u, abort)) return;
+            const uint32_t mt = sm.meta(jp);
             uint32_t flags, valid;
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(flags), "=r"(valid) : "r"(sm.meta(jp) + 1024u)
-                         : "memory");
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(flags), "=r"(valid) : "r"(mt + 1024u) : "memory");
             const bool first = flags & kFlagFirst, last = flags & kFlagLast;
             if (first) {
                 if (pending_epilogue) {  // the previous item's O must have been read out
@@ -514,15 +532,24 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                     pending_epilogue = false;
                 }
             } else if (flags & kFlagRescale) {
-                if (lane == 0) mma_commit(sm.bar(kBarMmaEvt));
+                // rescale event: per-head factors to the event buffer, then wait for the rows
+                asm volatile("{\n\t.reg .b32 x, y, z, w;\n\t"
+                             "ld.shared.v4.b32 {x, y, z, w}, [%0];\n\t"
+                             "st.shared.v4.b32 [%1], {x, y, z, w};\n\t}" ::"r"(mt + 16u * lane),
+                             "r"(evt + 16u * lane)
+                             : "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtRescale) : "memory");
+                    mbar_arrive(sm.bar(kBarMmaEvt));
+                    mma_commit(sm.bar(kBarMmaEvt));
+                }
                 __syncwarp();
                 if (!mbar_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
                 ++cv;
             }
-            for (int bx = 0; bx < kBoxesV; ++bx) {
-                uint32_t gg = g + bx;
-                if (!mbar_wait(sm.bar(kBarFull + gg % kRing), (gg / kRing) & 1u, abort)) return;
-            }
+            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStages) & 1u, abort)) return;
+            const uint32_t vb = sm.stage(s, kStageV);
             if (last && valid < (uint32_t)kPage) {
                 // rows past the end of the sequence may hold anything (even NaN): zero them,
                 // since 0 * NaN would poison O even though their probabilities are 0
@@ -530,7 +557,7 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                 for (uint32_t e = lane; e < nrow * 8u * kBoxesV; e += 32) {
                     uint32_t bx = e / (nrow * 8u), rem = e % (nrow * 8u);
                     uint32_t row = valid + rem / 8u, ch = rem % 8u;
-                    uint32_t addr = sm.ring((g + bx) % kRing) + row * 128u + ch * 16u;
+                    uint32_t addr = vb + bx * kBoxBytes + row * 128u + ch * 16u;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
                 fence_proxy_async_smem();
@@ -540,18 +567,31 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
             if (lane == 0) {
 #pragma unroll
                 for (int n = 0; n < 2; ++n) {
-                    const uint32_t vb = sm.ring((g + 4u * n) % kRing);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint64_t adesc = sdesc_sw128(sm.pbuf(jp) + 32u * k, 16u, 1024u);
-                        uint64_t bdesc = sdesc_sw128(vb + 2048u * k, (uint32_t)kBoxBytes, 1024u);
+                        uint64_t bdesc = sdesc_sw128(vb + 4u * n * kBoxBytes + 2048u * k, (uint32_t)kBoxBytes, 1024u);
                         mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, !(first && k == 0));
                     }
-#pragma unroll
-                    for (int bx = 0; bx < 4; ++bx) mma_commit(sm.bar(kBarEmpty + (g + 4u * n + bx) % kRing));
                 }
-                mma_commit_mc(sm.bar(kBarPFree + jp), (uint16_t)0x1);
-                if (last) mma_commit(sm.bar(kBarMmaEvt));
+                mma_commit(sm.bar(kBarEmpty + s));
+            }
+            if (last) {
+                // epilogue event: 1/l per head to the event buffer
+                asm volatile("{\n\t.reg .b32 x, y, z, w;\n\t"
+                             "ld.shared.v4.b32 {x, y, z, w}, [%0];\n\t"
+                             "st.shared.v4.b32 [%1], {x, y, z, w};\n\t}" ::"r"(mt + 512u + 16u * lane),
+                             "r"(evt + 512u + 16u * lane)
+                             : "memory");
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mma_commit_mc(sm.bar(kBarPFree + jp), (uint16_t)0x1);  // message consumed (meta read above)
+                if (last) {
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtEpilogue) : "memory");
+                    mbar_arrive(sm.bar(kBarMmaEvt));
+                    mma_commit(sm.bar(kBarMmaEvt));
+                }
             }
             __syncwarp();
             if (last) pending_epilogue = true;
@@ -560,13 +600,14 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
     if (pending_epilogue) mbar_wait(sm.bar(kBarCorrEvt), cv & 1u, abort);
 }
 
-// Accumulate CTA, epilogue warps (thread = head): rescale O on request, write the output.
+// Accumulate CTA, epilogue warps (thread = head): serve events -- rescale O rows, or
+// write the normalised output of the finished item.
 __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const Smem &sm, uint32_t tmem,
                                                     int cid, int ncl, int n_items, volatile int *abort) {
     const int h = threadIdx.x;  // 0..127
     const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
-    uint32_t pc = 0, ev = 0;
-    const uint32_t peer_free[2] = {mapa_shared(sm.bar(kBarPFree + 0), 0), mapa_shared(sm.bar(kBarPFree + 1), 0)};
+    const uint32_t evt = sm.evt();
+    uint32_t ev = 0;
     for (int r = 0;; ++r) {
         int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
@@ -576,22 +617,15 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
             for (int c = 0; c < kDc * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
             continue;
         }
-        for (int tile = it.tb; tile < it.te; ++tile, ++pc) {
-            const uint32_t jp = pc & 1u;
-            if (!mbar_wait<true>(sm.bar(kBarPFull + jp), (pc >> 1) & 1u, abort)) return;
-            const uint32_t mt = sm.meta(jp);
-            uint32_t flags;
-            float alpha, inv_l = 0.f;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(flags) : "r"(mt + 1024u) : "memory");
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(alpha) : "r"(mt + 4u * h) : "memory");
-            if (flags & kFlagLast)
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv_l) : "r"(mt + 512u + 4u * h) : "memory");
-            mbar_arrive_cluster(peer_free[jp]);  // this thread is done with the message
-
-            if (!(flags & kFlagFirst) && (flags & kFlagRescale)) {
-                if (!mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort)) return;
-                ++ev;
-                tc_fence_after();
+        for (;;) {
+            if (!mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort)) return;
+            ++ev;
+            tc_fence_after();
+            uint32_t type;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(type) : "r"(evt + 1024u) : "memory");
+            if (type == kEvtRescale) {
+                float alpha;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(alpha) : "r"(evt + 4u * h) : "memory");
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < kDc / 32; ++c) {
@@ -606,45 +640,45 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
                 }
                 tc_fence_before();
                 mbar_arrive(sm.bar(kBarCorrEvt));
+                continue;
             }
-            if (flags & kFlagLast) {
-                if (!mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort)) return;
-                ++ev;
-                tc_fence_after();
+            float inv_l;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv_l) : "r"(evt + 512u + 4u * h) : "memory");
 #pragma unroll 1
-                for (int c = 0; c < kDc / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + c * 32u, v);
-                    tmem_ld_wait();
-                    if (it.slot < 0) {
-                        uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + c * 32);
+            for (int c = 0; c < kDc / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + c * 32u, v);
+                tmem_ld_wait();
+                if (it.slot < 0) {
+                    uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + c * 32);
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv_l, __uint_as_float(v[8 * u + 1]) * inv_l);
-                            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv_l, __uint_as_float(v[8 * u + 3]) * inv_l);
-                            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv_l, __uint_as_float(v[8 * u + 5]) * inv_l);
-                            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv_l, __uint_as_float(v[8 * u + 7]) * inv_l);
-                            o[u] = w;
-                        }
-                    } else {
-                        float4 *o = reinterpret_cast<float4 *>(p.part_o + ((size_t)it.slot * kHeads + h) * kDc + c * 32);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            o[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
-                                               __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv_l, __uint_as_float(v[8 * u + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv_l, __uint_as_float(v[8 * u + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv_l, __uint_as_float(v[8 * u + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv_l, __uint_as_float(v[8 * u + 7]) * inv_l);
+                        o[u] = w;
                     }
+                } else {
+                    float4 *o = reinterpret_cast<float4 *>(p.part_o + ((size_t)it.slot * kHeads + h) * kDc + c * 32);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        o[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
+                                           __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
                 }
-                tc_fence_before();
-                mbar_arrive(sm.bar(kBarCorrEvt));
             }
+            tc_fence_before();
+            mbar_arrive(sm.bar(kBarCorrEvt));
+            break;
         }
     }
 }
 
 // Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates).
 __global__ void __launch_bounds__(192, 1)
-decode_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p) {
+decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_v,
+              const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
@@ -652,35 +686,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p)
     const int warp = threadIdx.x >> 5;
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x(), ncl = (int)nclusters_x();
-    volatile int *abort = reinterpret_cast<volatile int *>(smem_raw + (sm.base - raw) + kOffAbort);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + (sm.base - raw) + kOffTmemPtr);
-    volatile uint32_t *any_words = reinterpret_cast<volatile uint32_t *>(smem_raw + (sm.base - raw) + kOffAny);
+    uint8_t *const gbase = smem_raw + (sm.base - raw);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + kOffAbort);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemPtr);
+    volatile uint32_t *any_words = reinterpret_cast<volatile uint32_t *>(gbase + kOffAny);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRing; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(sm.bar(kBarFull + s), 1);
             mbar_init(sm.bar(kBarEmpty + s), 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(sm.bar(kBarSFull + j), 1);
             mbar_init(sm.bar(kBarSEmpty + j), 128);
-            mbar_init(sm.bar(kBarPFree + j), 129); // accumulate CTA: MMA commit + 128 epilogue releases
-            mbar_init(sm.bar(kBarPStaged + j), 128);
-            mbar_init(sm.bar(kBarPFull + j), 1);   // armed by the accumulate CTA's MMA warp
+        }
+        for (int j = 0; j < kPBufs; ++j) {
+            mbar_init(sm.bar(kBarPFree + j), 1);     // score CTA: the partner's MMA commit
+            mbar_init(sm.bar(kBarPFull + j), 1);     // accumulate CTA: armed by its MMA warp
+            mbar_init(sm.bar(kBarPStaged + j), 128); // score CTA: all rows written
+            any_words[j] = 0u;
         }
         mbar_init(sm.bar(kBarQReady), 128);
-        mbar_init(sm.bar(kBarMmaEvt), 1);
+        mbar_init(sm.bar(kBarMmaEvt), 2);            // MMA warp arrive + MMA commit
         mbar_init(sm.bar(kBarCorrEvt), 128);
         *abort = 0;
-        any_words[0] = 0u;
-        any_words[1] = 0u;
         fence_mbar_init();
     }
     if (warp == 5) {
         tmem_alloc(sm.base + kOffTmemPtr, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && (threadIdx.x & 31) == 0) tma_prefetch_desc(&tmap_kv);
+    if (warp == 4 && (threadIdx.x & 31) == 0) tma_prefetch_desc(rank == 0 ? &tmap_s : &tmap_v);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // the partner's barriers exist before any remote arrive or copy
@@ -689,8 +725,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p)
     const int n_items = p.hdr->n_items;
 
     if (warp == 4) {
-        if ((threadIdx.x & 31) == 0)
-            role_producer(p, &tmap_kv, sm, rank == 0 ? kBoxesS : kBoxesV, cid, ncl, n_items, abort);
+        if ((threadIdx.x & 31) == 0) {
+            if (rank == 0)
+                role_producer(p, &tmap_s, sm, kStageS, cid, ncl, n_items, abort);
+            else
+                role_producer(p, &tmap_v, sm, kStageV, cid, ncl, n_items, abort);
+        }
     } else if (warp == 5) {
         if (rank == 0) {
             if ((threadIdx.x & 31) == 0) role_score_mma(p, sm, tmem, cid, ncl, n_items, abort);

@@ -106,6 +106,20 @@ bool tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+// 3-D view of the latent page pool for whole-page TMA loads: (64 columns, rows, 9 column
+// blocks) with strides (2 B, 1152 B, 128 B).  A box of (64, 64, blocks) is one page's
+// first `blocks` 64-column blocks, landing as consecutive 8 KB swizzled blocks.
+bool tmap_pool_pages(CUtensorMap *m, const void *pool, uint64_t num_pages, uint32_t blocks) {
+    cuuint64_t dims[3] = {64, num_pages * kPage, (cuuint64_t)kBoxesS};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kPage, blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
@@ -268,8 +282,10 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
 
-    CUtensorMap tkv;
-    if (!tmap_2d(&tkv, kv_pool, kD, (uint64_t)num_pages * kPage, kD * 2, 64, kPage)) return MLA_ERR_CUDA;
+    CUtensorMap tmap_s, tmap_v;
+    if (!tmap_pool_pages(&tmap_s, kv_pool, (uint64_t)num_pages, kBoxesS) ||
+        !tmap_pool_pages(&tmap_v, kv_pool, (uint64_t)num_pages, kBoxesV))
+        return MLA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + w.hdr);
@@ -311,7 +327,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, decode_kernel, tkv, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, p) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
