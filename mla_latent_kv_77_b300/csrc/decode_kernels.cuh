@@ -7,19 +7,26 @@
 //
 // B300 design: one cluster of two CTAs (two SMs) per work item.
 //   CTA rank 0, the "score" CTA: holds the 128x576 absorbed query of the item in
-//     tensor memory (A operand, 288 columns), streams the 64-token pages with TMA
-//     (9 boxes of 64 tokens x 64 columns, 128-byte swizzle), computes
-//     S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05 into a
-//     double-buffered TMEM tile, runs the online softmax (one thread per head,
-//     lazy rescaling), and ships P (bf16, 128 x 64) plus per-head rescale factors
-//     to its partner with a shared->cluster bulk copy.
+//     tensor memory (A operand, 288 columns), streams the 64-token pages with one
+//     3-D TMA per page into a 3-stage ring (plus L2 prefetches further ahead),
+//     and computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05.
+//     Two MMA warps split each page's K range (column blocks 0-4 and 5-8) into
+//     two partial S tiles: one thread cannot issue N = 64 MMAs fast enough to
+//     keep the tensor pipe busy, two can, and a page then leaves its stage as
+//     soon as the tensor pipe is done with it.  Four softmax warps (thread =
+//     head) add the partials, run the online softmax with lazy rescaling and
+//     write P (bf16, 128 x 64) plus per-head factors straight from registers
+//     into a ring of messages in global memory (it stays in L2).
 //   CTA rank 1, the "accumulate" CTA: holds O = 128 heads x 512 latent fp32, i.e.
-//     all 512 TMEM columns, streams the same pages' 512 latent columns, and runs
-//     O += P V (M = 128, N = 256 x 2, K = 64) with tcgen05; its four epilogue
-//     warps rescale O when the partner asks, and write the normalised output.
+//     all 512 TMEM columns, streams the same pages' 512 latent columns (L2 hits:
+//     the score CTA has just pulled them from HBM), bulk-copies each P message
+//     into shared memory, and runs O += P V (M = 128, N = 256 x 2, K = 64); its
+//     four epilogue warps rescale O when asked and write the normalised output.
 // The split keeps both 256 KB accumulators on chip without recomputing S: O alone
 // fills a whole SM's tensor memory, and the query alone would fill most of its
-// shared memory.
+// shared memory.  P travels through L2 rather than distributed shared memory,
+// whose bandwidth between the two SMs of a pair is far below what one 16 KB
+// message per page needs; only the small ready/free signals are remote arrives.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,47 +45,56 @@ constexpr int kBoxBytes = kPage * 128;  // one 64-row x 64-column bf16 block (12
 constexpr int kBoxesS = kD / 64;     // 9 blocks per page for scoring (c and k^R)
 constexpr int kBoxesV = kDc / 64;    // 8 blocks per page for the value side (c only)
 constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page
-constexpr uint32_t kStageV = kBoxesV * kBoxBytes;  // 65536: a page's latent columns
-constexpr int kStages = 2;           // page stages per CTA
-constexpr int kPBufs = 4;            // P messages in flight between the two CTAs
+constexpr uint32_t kStageV = kBoxesV / 2 * kBoxBytes;  // 32768: half of a page's latent columns
+constexpr int kStagesS = 3;          // score CTA page stages
+constexpr int kStagesV = 4;          // accumulate CTA half-page stages (two per page)
+constexpr int kPBufs = 4;            // accumulate CTA: P messages held in shared memory
+constexpr int kRing = 16;            // P messages in flight through global memory, per CTA pair
+constexpr int kBatch = 4;            // messages published together (one cluster-scope release each)
+constexpr int kRingBatches = kRing / kBatch;
+constexpr int kPrefetch = 6;         // pages prefetched into L2 ahead of the page being loaded
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
-constexpr int kMetaBytes = 1040;     // alpha[128] f32, inv_l[128] f32, flags, valid, pad
-constexpr int kMetaStride = 1088;
+constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
+constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one ring slot in global memory
 constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (factor 256)
+constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns
-constexpr uint32_t kTmemS = 0;       // score CTA: S buffers at 0 and 64
+constexpr uint32_t kTmemS = 0;       // score CTA: the page's two partial S tiles at 0 and 64
 constexpr uint32_t kTmemQ = 128;     // score CTA: Q (bf16 pairs) at 128 .. 415
 constexpr uint32_t kTmemCols = 512;
 
-// Shared memory (offsets from a 1024-aligned base).  The message area and the barriers sit
-// at the same offsets in both CTAs (the partner addresses them remotely); the page stages
-// follow, 72 KB each in the score CTA and 64 KB each in the accumulate CTA.
-constexpr uint32_t kOffP = 0;                                       // kPBufs x 16 KB
-constexpr uint32_t kOffMeta = kOffP + kPBufs * kPBytes;             // kPBufs x 1088
-constexpr uint32_t kOffEvt = kOffMeta + kPBufs * kMetaStride;       // alpha[128], inv_l[128], type
-constexpr uint32_t kOffBar = kOffEvt + 1040;
-constexpr int kBarFull = 0;
-constexpr int kBarEmpty = kBarFull + kStages;
-constexpr int kBarSFull = kBarEmpty + kStages;
-constexpr int kBarSEmpty = kBarSFull + 2;
-constexpr int kBarQReady = kBarSEmpty + 2;
-constexpr int kBarPFree = kBarQReady + 1;
-constexpr int kBarPFull = kBarPFree + kPBufs;
-constexpr int kBarPStaged = kBarPFull + kPBufs;
-constexpr int kBarMmaEvt = kBarPStaged + kPBufs;
-constexpr int kBarCorrEvt = kBarMmaEvt + 1;
+// Shared memory (offsets from a 1024-aligned base).  Score CTA: page stages at 0.
+// Accumulate CTA: half-page stages at 0, P buffers, their factors, the event buffer.
+// Barriers sit at the same offset in both CTAs (the partner arrives on them).
+constexpr uint32_t kOffPBuf = kStagesV * kStageV;                   // accumulate: kPBufs x 16 KB
+constexpr uint32_t kOffMeta = kOffPBuf + kPBufs * kPBytes;          // accumulate: kPBufs x 1 KB
+constexpr uint32_t kOffEvt = kOffMeta + kPBufs * kMetaBytes;        // accumulate: alpha / inv_l, type
+constexpr uint32_t kAccumEnd = kOffEvt + 1040;
+constexpr uint32_t kScoreEnd = kStagesS * kStageS;
+constexpr uint32_t kOffBar = kScoreEnd > kAccumEnd ? kScoreEnd : kAccumEnd;
+constexpr int kStagesMax = kStagesS > kStagesV ? kStagesS : kStagesV;
+constexpr int kBarFull = 0;                          // page stages (score) / half-page stages (accumulate)
+constexpr int kBarEmpty = kBarFull + kStagesMax;
+constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: partial S tile written (one per issuer)
+constexpr int kBarSEmpty = kBarSFull + 2;            // score: both partial tiles read by the softmax warps
+constexpr int kBarQReady = kBarSEmpty + 1;           // score: the item's Q is in TMEM
+constexpr int kBarPFree = kBarQReady + 1;            // score: ring slot consumed (partner arrives)
+constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a batch of ring slots written (partner arrives)
+constexpr int kBarPStaged = kBarPReady + kRingBatches;  // score: all rows of a ring slot written
+constexpr int kBarPFull = kBarPStaged + kRing;       // accumulate: P buffer landed
+constexpr int kBarPBufFree = kBarPFull + kPBufs;     // accumulate: P buffer used by the MMAs and the releaser
+constexpr int kBarMmaEvt = kBarPBufFree + kPBufs;    // accumulate: event for the epilogue warps
+constexpr int kBarCorrEvt = kBarMmaEvt + 1;          // accumulate: event served
 constexpr int kNumBars = kBarCorrEvt + 1;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kOffAny = kOffAbort + 4;  // kPBufs words: OR of the rescale requests per message
-constexpr uint32_t kOffStages = (kOffAny + 4 * kPBufs + 1023u) & ~1023u;
-constexpr uint32_t kDecodeSmem = kOffStages + kStages * kStageS + 1024;  // + slack to align the base
+constexpr uint32_t kDecodeSmem = kOffAbort + 16 + 1024;  // + slack to align the base
+constexpr int kDecodeThreads = 256;  // 4 softmax/epilogue warps, producer, 2 MMA/loader warps, shipper/releaser
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);    // A = Q (TMEM), B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A = P K-major, B = V MN-major
 
-constexpr uint32_t kFlagFirst = 1u, kFlagRescale = 2u, kFlagLast = 4u;
 constexpr uint32_t kEvtRescale = 1u, kEvtEpilogue = 2u;
 
 // One unit of work: tiles [tb, te) of query (b, t) where bt = b * Tq + t.
@@ -109,6 +125,7 @@ struct DecodeParams {
     const Item *items;
     float *part_o;                // [slots, 128, 512]
     float *part_lse;              // [slots, 128]
+    uint8_t *ring;                // [clusters, kRing, kMsgBytes] P messages
     int B, Tq, causal, num_pages, max_pages;
     float sl2;                    // scale * log2(e)
 };
@@ -298,9 +315,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
 struct Smem {
     uint32_t base;  // shared::cta address of the aligned base
     __device__ __forceinline__ uint32_t bar(int i) const { return base + kOffBar + 8u * i; }
-    __device__ __forceinline__ uint32_t stage(uint32_t s, uint32_t bytes) const { return base + kOffStages + s * bytes; }
-    __device__ __forceinline__ uint32_t pbuf(uint32_t j) const { return base + kOffP + j * kPBytes; }
-    __device__ __forceinline__ uint32_t meta(uint32_t j) const { return base + kOffMeta + j * kMetaStride; }
+    __device__ __forceinline__ uint32_t stage(uint32_t s, uint32_t bytes) const { return base + s * bytes; }
+    __device__ __forceinline__ uint32_t pbuf(uint32_t j) const { return base + kOffPBuf + j * kPBytes; }
+    __device__ __forceinline__ uint32_t meta(uint32_t j) const { return base + kOffMeta + j * kMetaBytes; }
     __device__ __forceinline__ uint32_t evt() const { return base + kOffEvt; }
 };
 
@@ -312,80 +329,161 @@ __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
-
-// Producer: one TMA per page.  The tensor map views the pool as (64 columns, rows, column
-// blocks) with strides (2 B, 1152 B, 128 B), so a single box lands in shared memory as
-// `blocks` consecutive 64-row x 128-byte swizzled blocks -- the operand layout of the MMAs.
-__device__ __forceinline__ void role_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                              uint32_t stage_bytes, int cid, int ncl, int n_items,
-                                              volatile int *abort) {
-    uint32_t g = 0;
-    for (int r = 0;; ++r) {
-        int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        ItemInfo it = load_item(p, i);
-        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            int pg = p.block_table[(size_t)it.b * p.max_pages + tile];
-            if (pg < 0 || pg >= p.num_pages) {
-                raise_status(0x1u);
-                pg = 0;
-            }
-            const uint32_t s = g % kStages;
-            if (!mbar_wait(sm.bar(kBarEmpty + s), ((g / kStages) & 1u) ^ 1u, abort)) return;
-            mbar_arrive_expect_tx(sm.bar(kBarFull + s), stage_bytes);
-            tma_load_3d(sm.stage(s, stage_bytes), tmap, 0, pg * kPage, 0, sm.bar(kBarFull + s));
-        }
-    }
-    // let every load issued land before the CTA can retire (bounded)
-    for (uint32_t k = (g > kStages ? g - kStages : 0); k < g; ++k)
-        if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+// global -> shared::cta bulk copy, completion counted on a local barrier
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// arrive on a barrier of another CTA with no ordering of this thread's memory operations
+// (a pure "slot consumed" signal; nothing written by this thread is published by it)
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-// Score CTA, MMA issuer (one thread): S_j = Q . K_tile^T, K = 576 in 36 steps.
-__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
-                                               int ncl, int n_items, volatile int *abort) {
+__device__ __forceinline__ int checked_page(const DecodeParams &p, int b, int tile) {
+    int pg = p.block_table[(size_t)b * p.max_pages + tile];
+    if (pg < 0 || pg >= p.num_pages) {
+        raise_status(0x1u);
+        pg = 0;
+    }
+    return pg;
+}
+
+// Waits whose lanes must stay converged (warp-collective instructions follow): lane 0 waits,
+// the outcome is broadcast, and on a failed wait the whole warp leaves together.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+// Every lane waits; if any lane of the warp gave up, the whole warp gives up.
+#define MLA_WAIT_WARP(expr) \
+    if (__any_sync(0xffffffffu, !(expr))) return
+
+// Page producer (a whole warp; lane 0 issues).  The tensor map views the pool as (64 columns,
+// rows, column blocks) with strides (2 B, 1152 B, 128 B), so one box lands in shared memory as
+// `blocks` consecutive 64-row x 128-byte swizzled blocks -- the operand layout of the MMAs.
+// Block-table entries are read 32 tiles at a time (one per lane) and one chunk ahead.  With
+// `prefetch`, each load also asks L2 for the page kPrefetch tiles further on.
+// kHalves = 2: each page is loaded as two half-page boxes (latent blocks 0-3 and 4-7) into
+// consecutive stages, so the value MMAs of one half can start and release independently.
+template <int kStages, int kHalves>
+__device__ __forceinline__ void role_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
+                                              uint32_t stage_bytes, bool prefetch, int cid, int ncl, int n_items,
+                                              volatile int *abort) {
+    const int lane = threadIdx.x & 31;
+    uint32_t g = 0;
+    for (int r = 0;; ++r) {
+        const int i = schedule(r, cid, ncl);
+        if (i >= n_items) break;
+        const ItemInfo it = load_item(p, i);
+        int cur = it.tb + lane < it.te ? checked_page(p, it.b, it.tb + lane) : 0;
+        int nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
+        int chunk = it.tb;
+        if (prefetch) {  // the item's first pages
+            const int pf = it.tb + (lane < kPrefetch ? lane : 0);
+            const int pg = __shfl_sync(0xffffffffu, cur, pf - it.tb);
+            if (lane < kPrefetch && pf < it.te) tma_prefetch_l2_3d(tmap, 0, pg * kPage, 0);
+        }
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            if (tile - chunk == 32) {
+                chunk += 32;
+                cur = nxt;
+                nxt = chunk + 32 + lane < it.te ? checked_page(p, it.b, chunk + 32 + lane) : 0;
+            }
+            const int idx = tile - chunk;
+            const int pg = __shfl_sync(0xffffffffu, cur, idx);
+            const int fidx = idx + kPrefetch;
+            const int fpg = __shfl_sync(0xffffffffu, fidx < 32 ? cur : nxt, fidx & 31);
+#pragma unroll
+            for (int hf = 0; hf < kHalves; ++hf) {
+                const uint32_t u = g * kHalves + hf, s = u % kStages;
+                if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStages) & 1u) ^ 1u, abort)) return;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(sm.bar(kBarFull + s), stage_bytes);
+                    tma_load_3d(sm.stage(s, stage_bytes), tmap, 0, pg * kPage, hf * (kBoxesV / 2),
+                                sm.bar(kBarFull + s));
+                }
+                __syncwarp();
+            }
+            if (lane == 0 && prefetch && tile + kPrefetch < it.te) tma_prefetch_l2_3d(tmap, 0, fpg * kPage, 0);
+        }
+    }
+    g *= kHalves;
+    // let every load issued land before the CTA can retire (bounded)
+    if (lane == 0)
+        for (uint32_t k = (g > kStages ? g - kStages : 0); k < g; ++k)
+            if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
+}
+
+// Score CTA, MMA issuer `me` (0 or 1, one thread each).  Both issuers work on every page:
+// issuer 0 accumulates column blocks 0-4 of S = Q . K_tile^T into partial tile 0, issuer 1
+// blocks 5-8 into partial tile 1, each in fully unrolled steps with constant descriptor
+// offsets.  The page's stage is free once both have committed.
+__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, uint32_t me,
+                                               int cid, int ncl, int n_items, volatile int *abort) {
+    constexpr int kSplit = 5;  // column blocks of issuer 0
     uint32_t g = 0, ic = 0;
     for (int r = 0;; ++r) {
-        int i = schedule(r, cid, ncl);
+        const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
-        ItemInfo it = load_item(p, i);
+        const ItemInfo it = load_item(p, i);
         if (it.te <= it.tb) continue;
         if (!mbar_wait(sm.bar(kBarQReady), ic & 1u, abort)) return;
         tc_fence_after();
         ++ic;
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            const uint32_t j = g & 1u, s = g % kStages;
-            if (!mbar_wait(sm.bar(kBarSEmpty + j), ((g >> 1) & 1u) ^ 1u, abort)) return;
-            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStages) & 1u, abort)) return;
+            const uint32_t s = g % kStagesS;
+            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStagesS) & 1u, abort)) return;
+            if (!mbar_wait(sm.bar(kBarSEmpty), (g & 1u) ^ 1u, abort)) return;
             tc_fence_after();
-            const uint32_t d = tmem + kTmemS + j * 64u;
-            const uint32_t kb = sm.stage(s, kStageS);
-#pragma unroll 1
-            for (int bx = 0; bx < kBoxesS; ++bx) {
+            const uint32_t d = tmem + kTmemS + me * 64u;
+            const uint64_t b0 = sdesc_sw128(sm.stage(s, kStageS), 16u, 1024u);
+            if (me == 0) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint64_t bdesc = sdesc_sw128(kb + bx * kBoxBytes + 32u * k, 16u, 1024u);
-                    mma_ts(d, tmem + kTmemQ + bx * 32u + k * 8u, bdesc, kIdescS, (bx | k) != 0);
+                for (int k = 0; k < 4 * kSplit; ++k) {
+                    const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
+                    mma_ts(d, tmem + kTmemQ + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4),
+                           kIdescS, k != 0);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4 * (kBoxesS - kSplit); ++k) {
+                    const uint32_t bx = kSplit + ((uint32_t)k >> 2), kk = (uint32_t)k & 3u;
+                    mma_ts(d, tmem + kTmemQ + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4),
+                           kIdescS, k != 0);
                 }
             }
             mma_commit(sm.bar(kBarEmpty + s));
-            mma_commit(sm.bar(kBarSFull + j));
+            mma_commit(sm.bar(kBarSFull + me));
         }
     }
 }
 
-// Score CTA, softmax warps (thread = head).
+// Score CTA, softmax warps (thread = head).  Per page: read S, online softmax with lazy
+// rescaling, write the P message (bf16 row in the UMMA K-major 128-byte-swizzle image,
+// the rescale factor, and 1/l on the item's last page) into the ring, then signal.
 __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
-                                             int ncl, int n_items, volatile int *abort,
-                                             volatile uint32_t *any_words) {
+                                             int ncl, int n_items, volatile int *abort) {
     const int h = threadIdx.x;  // 0..127
     const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
     const float sl2 = p.sl2;
+    const uint32_t row_off = (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u;
+    uint8_t *const ring = p.ring + (size_t)cid * kRing * kMsgBytes;
     uint32_t sc = 0;
     for (int r = 0;; ++r) {
-        int i = schedule(r, cid, ncl);
+        const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
-        ItemInfo it = load_item(p, i);
+        const ItemInfo it = load_item(p, i);
         if (it.te <= it.tb) {
             p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
             continue;
@@ -412,33 +510,41 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
         }
         float m = 0.f, l = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
-            const uint32_t j = sc & 1u;
-            if (!mbar_wait(sm.bar(kBarSFull + j), (sc >> 1) & 1u, abort)) return;
+            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarSFull + 0), sc & 1u, abort));
+            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarSFull + 1), sc & 1u, abort));
             tc_fence_after();
-            uint32_t sr[64];
+            float s[64];
             {
-                uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                tmem_ld32(tmem + lane_off + kTmemS + j * 64u, a);
-                tmem_ld32(tmem + lane_off + kTmemS + j * 64u + 32u, b);
+                uint32_t a[32], b[32];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    tmem_ld32(tmem + lane_off + kTmemS + 32u * hf, a);
+                    tmem_ld32(tmem + lane_off + kTmemS + 64u + 32u * hf, b);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[32 * hf + c] = __uint_as_float(a[c]) + __uint_as_float(b[c]);
+                }
             }
-            tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(sm.bar(kBarSEmpty + j));
+            mbar_arrive(sm.bar(kBarSEmpty));
 
             const int valid = min(kPage, it.n_vis - tile * kPage);
-            float s[64];
-            float mx = -INFINITY;
+            if (valid < kPage) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float v = c < valid ? __uint_as_float(sr[c]) : -INFINITY;
-                s[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
             }
-            mx *= sl2;
+            // row max as a tree (fmaxf is exact, so the order does not matter)
+            float mx4[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float a = s[16 * q4];
+#pragma unroll
+                for (int c = 1; c < 16; ++c) a = fmaxf(a, s[16 * q4 + c]);
+                mx4[q4] = a;
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
             const bool first = tile == it.tb;
             const bool last = tile == it.te - 1;
-            bool resc = false;
             float alpha = 1.f;
             if (first) {
                 m = mx;
@@ -446,59 +552,109 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 alpha = ex2_approx(m - mx);
                 l *= alpha;
                 m = mx;
-                resc = true;
             }
             uint32_t pk[32];
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
-                float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
+                const float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
+                const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
                 pk[c] = pack_bf16x2(a, b);
-                lsum += a + b;  // the row sum uses the unrounded probabilities (exact lse)
+                ls[c & 3] += a + b;  // the row sum uses the unrounded probabilities (exact lse)
             }
-            l += lsum;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
-            // ship P, alpha (and 1/l on the last tile) to the accumulate CTA
-            const uint32_t jp = sc % kPBufs, use = sc / kPBufs;
-            if (!mbar_wait<true>(sm.bar(kBarPFree + jp), (use & 1u) ^ 1u, abort)) return;
-            {
-                const uint32_t row = sm.pbuf(jp) + (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u;
+            // the message, straight into its ring slot once the partner has taken the slot's
+            // previous content (a plain signal: that copy completed before the partner
+            // arrived): P row in the UMMA K-major 128-byte-swizzle image, the rescale factor,
+            // and 1/l on the item's last page
+            const uint32_t rs = sc % kRing;
+            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarPFree + rs), ((sc / kRing) & 1u) ^ 1u, abort));
+            uint8_t *msg = ring + (size_t)rs * kMsgBytes;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t addr = row + (uint32_t)((c ^ (h & 7)) * 16);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]),
-                                 "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                 : "memory");
-                }
-                const uint32_t mt = sm.meta(jp);
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(mt + 4u * h), "f"(alpha) : "memory");
-                if (last)
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(mt + 512u + 4u * h), "f"(1.0f / l) : "memory");
+            for (int c = 0; c < 8; ++c) {
+                uint4 *dst = reinterpret_cast<uint4 *>(msg + row_off + (uint32_t)((c ^ (h & 7)) * 16));
+                *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
-            if (resc) atomicOr(const_cast<unsigned int *>(any_words + jp), 1u);
-            fence_proxy_async_smem();
-            mbar_arrive(sm.bar(kBarPStaged + jp));
-            if (h == 0) {
-                // all 128 rows staged: send the message (bounded wait, no hardware barrier)
-                if (!mbar_wait(sm.bar(kBarPStaged + jp), use & 1u, abort)) return;
-                const uint32_t any = any_words[jp];
-                any_words[jp] = 0u;
-                const uint32_t flags = (first ? kFlagFirst : 0u) | (any ? kFlagRescale : 0u) | (last ? kFlagLast : 0u);
-                const uint32_t mt = sm.meta(jp);
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mt + 1024u), "r"(flags), "r"((uint32_t)valid)
-                             : "memory");
-                fence_proxy_async_smem();
-                const uint32_t peer_full = mapa_shared(sm.bar(kBarPFull + jp), 1);
-                bulk_copy_s2c(mapa_shared(sm.pbuf(jp), 1), sm.pbuf(jp), kPBytes, peer_full);
-                bulk_copy_s2c(mapa_shared(mt, 1), mt, kMetaBytes, peer_full);
-            }
+            reinterpret_cast<float *>(msg + kPBytes)[h] = alpha;
+            if (last) reinterpret_cast<float *>(msg + kPBytes)[kHeads + h] = 1.0f / l;
+            // local release; the shipper publishes the slot to the partner
+            mbar_arrive(sm.bar(kBarPStaged + rs));
         }
         const float lse = (m + __log2f(l)) * 0.69314718055994531f;
         if (it.slot < 0)
             p.lse[(size_t)it.bt * kHeads + h] = lse;
         else
             p.part_lse[(size_t)it.slot * kHeads + h] = lse;
+    }
+}
+
+// Score CTA, shipper (one thread): publishes the ring slots the softmax warps have written
+// to the partner, kBatch at a time, with one cluster-scope release per batch.  It acquires
+// the rows through the local barrier, and release/acquire chains are transitive, so the
+// partner's acquire sees every row.  Such a release waits for the rows' stores to complete
+// and costs about a microsecond here, too much to pay per message; and the compute warps
+// never touch a cluster-scope barrier.
+static_assert(kRing % kBatch == 0 && kRingBatches >= 3, "ring must hold at least three batches");
+__device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
+                                             volatile int *abort) {
+    uint32_t g = 0;
+    for (int r = 0;; ++r) {
+        const int i = schedule(r, cid, ncl);
+        if (i >= n_items) break;
+        const ItemInfo it = load_item(p, i);
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            if (!mbar_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
+            if ((g + 1) % kBatch == 0)
+                mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
+        }
+    }
+    if (g % kBatch != 0)  // the last, partial batch
+        mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
+}
+
+// Accumulate CTA, releaser (one thread): hands each ring slot back to the partner as soon as
+// its message has landed in shared memory, off the MMA warp's path.  Its local arrival is
+// the second one each P buffer needs before the loader refills it, so this thread can never
+// fall a whole buffer cycle behind the barrier it watches.
+__device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
+                                              volatile int *abort) {
+    uint32_t g = 0;
+    for (int r = 0;; ++r) {
+        const int i = schedule(r, cid, ncl);
+        if (i >= n_items) break;
+        const ItemInfo it = load_item(p, i);
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            if (!mbar_wait(sm.bar(kBarPFull + g % kPBufs), (g / kPBufs) & 1u, abort)) return;
+            mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPFree + g % kRing), 0));
+            mbar_arrive(sm.bar(kBarPBufFree + g % kPBufs));
+        }
+    }
+}
+
+// Accumulate CTA, P loader (one thread): ring slot -> shared P buffer, as soon as the
+// partner has written it and the buffer's previous message has been used.
+__device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
+                                              volatile int *abort) {
+    const uint8_t *ring = p.ring + (size_t)cid * kRing * kMsgBytes;
+    uint32_t g = 0;
+    for (int r = 0;; ++r) {
+        const int i = schedule(r, cid, ncl);
+        if (i >= n_items) break;
+        const ItemInfo it = load_item(p, i);
+        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            const uint32_t rs = g % kRing, jp = g % kPBufs;
+            if (g % kBatch == 0) {  // a new batch: wait until the partner has published it
+                const uint32_t b = g / kBatch;
+                if (!mbar_wait<true>(sm.bar(kBarPReady + b % kRingBatches), (b / kRingBatches) & 1u, abort)) return;
+                fence_proxy_async_global();  // the partner's writes, before our async-proxy reads
+            }
+            if (!mbar_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
+            mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
+            const uint8_t *msg = ring + (size_t)rs * kMsgBytes;
+            bulk_load_g2s(sm.pbuf(jp), msg, kPBytes, sm.bar(kBarPFull + jp));
+            bulk_load_g2s(sm.meta(jp), msg + kPBytes, kMetaBytes, sm.bar(kBarPFull + jp));
+        }
     }
 }
 
@@ -513,68 +669,74 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
     bool pending_epilogue = false;
     const uint32_t evt = sm.evt();
     for (int r = 0;; ++r) {
-        int i = schedule(r, cid, ncl);
+        const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
-        ItemInfo it = load_item(p, i);
+        const ItemInfo it = load_item(p, i);
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            const uint32_t jp = g % kPBufs, use = g / kPBufs, s = g % kStages;
-            if (lane == 0) mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kPBytes + kMetaBytes);
-            __syncwarp();
-            if (!mbar_wait<true>(sm.bar(kBarPFull + jp), use & 1u, abort)) return;
+            const uint32_t jp = g % kPBufs;
+            const bool first = tile == it.tb, last = tile == it.te - 1;
+            const uint32_t valid = (uint32_t)min(kPage, it.n_vis - tile * kPage);
+            if (!warp_wait(sm.bar(kBarPFull + jp), (g / kPBufs) & 1u, abort)) return;
             const uint32_t mt = sm.meta(jp);
-            uint32_t flags, valid;
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(flags), "=r"(valid) : "r"(mt + 1024u) : "memory");
-            const bool first = flags & kFlagFirst, last = flags & kFlagLast;
             if (first) {
                 if (pending_epilogue) {  // the previous item's O must have been read out
-                    if (!mbar_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
+                    if (!warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
                     ++cv;
                     pending_epilogue = false;
                 }
-            } else if (flags & kFlagRescale) {
-                // rescale event: per-head factors to the event buffer, then wait for the rows
-                asm volatile("{\n\t.reg .b32 x, y, z, w;\n\t"
-                             "ld.shared.v4.b32 {x, y, z, w}, [%0];\n\t"
-                             "st.shared.v4.b32 [%1], {x, y, z, w};\n\t}" ::"r"(mt + 16u * lane),
-                             "r"(evt + 16u * lane)
+            } else {
+                float4 a4;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(a4.x), "=f"(a4.y), "=f"(a4.z), "=f"(a4.w)
+                             : "r"(mt + 16u * lane)
                              : "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtRescale) : "memory");
-                    mbar_arrive(sm.bar(kBarMmaEvt));
-                    mma_commit(sm.bar(kBarMmaEvt));
-                }
-                __syncwarp();
-                if (!mbar_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
-                ++cv;
-            }
-            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStages) & 1u, abort)) return;
-            const uint32_t vb = sm.stage(s, kStageV);
-            if (last && valid < (uint32_t)kPage) {
-                // rows past the end of the sequence may hold anything (even NaN): zero them,
-                // since 0 * NaN would poison O even though their probabilities are 0
-                const uint32_t nrow = kPage - valid;
-                for (uint32_t e = lane; e < nrow * 8u * kBoxesV; e += 32) {
-                    uint32_t bx = e / (nrow * 8u), rem = e % (nrow * 8u);
-                    uint32_t row = valid + rem / 8u, ch = rem % 8u;
-                    uint32_t addr = vb + bx * kBoxBytes + row * 128u + ch * 16u;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            tc_fence_after();
-            if (lane == 0) {
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint64_t adesc = sdesc_sw128(sm.pbuf(jp) + 32u * k, 16u, 1024u);
-                        uint64_t bdesc = sdesc_sw128(vb + 4u * n * kBoxBytes + 2048u * k, (uint32_t)kBoxBytes, 1024u);
-                        mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, !(first && k == 0));
+                const bool any = __any_sync(0xffffffffu, a4.x != 1.f || a4.y != 1.f || a4.z != 1.f || a4.w != 1.f);
+                if (any) {
+                    // rescale event: per-head factors to the event buffer, then wait for the rows
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(evt + 16u * lane), "f"(a4.x),
+                                 "f"(a4.y), "f"(a4.z), "f"(a4.w)
+                                 : "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtRescale) : "memory");
+                        mbar_arrive(sm.bar(kBarMmaEvt));
+                        mma_commit(sm.bar(kBarMmaEvt));
                     }
+                    __syncwarp();
+                    if (!warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
+                    ++cv;
                 }
-                mma_commit(sm.bar(kBarEmpty + s));
+            }
+            const uint64_t a0 = sdesc_sw128(sm.pbuf(jp), 16u, 1024u);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const uint32_t u = 2u * g + n, s = u % kStagesV;
+                if (!warp_wait(sm.bar(kBarFull + s), (u / kStagesV) & 1u, abort)) return;
+                const uint32_t vb = sm.stage(s, kStageV);
+                if (last && valid < (uint32_t)kPage) {
+                    // rows past the end of the sequence may hold anything (even NaN): zero them,
+                    // since 0 * NaN would poison O even though their probabilities are 0
+                    const uint32_t nrow = kPage - valid;
+                    for (uint32_t e = lane; e < nrow * 8u * (kBoxesV / 2); e += 32) {
+                        uint32_t bx = e / (nrow * 8u), rem = e % (nrow * 8u);
+                        uint32_t row = valid + rem / 8u, ch = rem % 8u;
+                        uint32_t addr = vb + bx * kBoxBytes + row * 128u + ch * 16u;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t v0 = sdesc_sw128(vb, (uint32_t)kBoxBytes, 1024u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss(tmem + 256u * n, a0 + (uint64_t)((32u * k) >> 4), v0 + (uint64_t)((2048u * k) >> 4),
+                               kIdescPV, !(first && k == 0));
+                    mma_commit(sm.bar(kBarEmpty + s));
+                    if (n == 1) mma_commit(sm.bar(kBarPBufFree + jp));
+                }
+                __syncwarp();
             }
             if (last) {
                 // epilogue event: 1/l per head to the event buffer
@@ -583,21 +745,18 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                              "st.shared.v4.b32 [%1], {x, y, z, w};\n\t}" ::"r"(mt + 512u + 16u * lane),
                              "r"(evt + 512u + 16u * lane)
                              : "memory");
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mma_commit_mc(sm.bar(kBarPFree + jp), (uint16_t)0x1);  // message consumed (meta read above)
-                if (last) {
+                __syncwarp();
+                if (lane == 0) {
                     asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtEpilogue) : "memory");
                     mbar_arrive(sm.bar(kBarMmaEvt));
                     mma_commit(sm.bar(kBarMmaEvt));
                 }
+                pending_epilogue = true;
             }
             __syncwarp();
-            if (last) pending_epilogue = true;
         }
     }
-    if (pending_epilogue) mbar_wait(sm.bar(kBarCorrEvt), cv & 1u, abort);
+    if (pending_epilogue) warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort);
 }
 
 // Accumulate CTA, epilogue warps (thread = head): serve events -- rescale O rows, or
@@ -609,16 +768,16 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
     const uint32_t evt = sm.evt();
     uint32_t ev = 0;
     for (int r = 0;; ++r) {
-        int i = schedule(r, cid, ncl);
+        const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
-        ItemInfo it = load_item(p, i);
+        const ItemInfo it = load_item(p, i);
         if (it.te <= it.tb) {
             uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc);
             for (int c = 0; c < kDc * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
             continue;
         }
         for (;;) {
-            if (!mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort)) return;
+            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort));
             ++ev;
             tc_fence_after();
             uint32_t type;
@@ -675,8 +834,11 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
     }
 }
 
-// Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates).
-__global__ void __launch_bounds__(192, 1)
+// Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates), 256 threads:
+// warps 0-3 softmax (rank 0) / epilogue (rank 1), warp 4 page producer, warps 5-6 the two
+// score MMA issuers (rank 0) / the PV MMA warp and the P loader (rank 1), warp 7 the
+// message shipper (rank 0) / the ring-slot releaser (rank 1).
+__global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_v,
               const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -689,24 +851,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     uint8_t *const gbase = smem_raw + (sm.base - raw);
     volatile int *abort = reinterpret_cast<volatile int *>(gbase + kOffAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemPtr);
-    volatile uint32_t *any_words = reinterpret_cast<volatile uint32_t *>(gbase + kOffAny);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStagesMax; ++s) {
             mbar_init(sm.bar(kBarFull + s), 1);
-            mbar_init(sm.bar(kBarEmpty + s), 1);
+            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? 2 : 1);  // score: both issuers commit
         }
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(sm.bar(kBarSFull + j), 1);
-            mbar_init(sm.bar(kBarSEmpty + j), 128);
-        }
-        for (int j = 0; j < kPBufs; ++j) {
-            mbar_init(sm.bar(kBarPFree + j), 1);     // score CTA: the partner's MMA commit
-            mbar_init(sm.bar(kBarPFull + j), 1);     // accumulate CTA: armed by its MMA warp
-            mbar_init(sm.bar(kBarPStaged + j), 128); // score CTA: all rows written
-            any_words[j] = 0u;
-        }
+        for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
+        mbar_init(sm.bar(kBarSEmpty), 128);
         mbar_init(sm.bar(kBarQReady), 128);
+        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPFree + j), 1);  // score CTA: the partner's releaser
+        for (int j = 0; j < kRingBatches; ++j) mbar_init(sm.bar(kBarPReady + j), 1);  // accumulate CTA: the shipper
+        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPStaged + j), 128);  // score CTA: softmax threads
+        for (int j = 0; j < kPBufs; ++j) {
+            mbar_init(sm.bar(kBarPFull + j), 1);     // accumulate CTA: armed by the P loader
+            mbar_init(sm.bar(kBarPBufFree + j), 2);  // accumulate CTA: MMA commit + releaser
+        }
         mbar_init(sm.bar(kBarMmaEvt), 2);            // MMA warp arrive + MMA commit
         mbar_init(sm.bar(kBarCorrEvt), 128);
         *abort = 0;
@@ -719,34 +879,41 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     if (warp == 4 && (threadIdx.x & 31) == 0) tma_prefetch_desc(rank == 0 ? &tmap_s : &tmap_v);
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // the partner's barriers exist before any remote arrive or copy
+    cluster_sync_all();  // the partner's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int n_items = p.hdr->n_items;
 
     if (warp == 4) {
+        if (rank == 0)
+            role_producer<kStagesS, 1>(p, &tmap_s, sm, kStageS, true, cid, ncl, n_items, abort);
+        else
+            role_producer<kStagesV, 2>(p, &tmap_v, sm, kStageV, false, cid, ncl, n_items, abort);
+    } else if (warp == 7) {
         if ((threadIdx.x & 31) == 0) {
             if (rank == 0)
-                role_producer(p, &tmap_s, sm, kStageS, cid, ncl, n_items, abort);
+                role_shipper(p, sm, cid, ncl, n_items, abort);
             else
-                role_producer(p, &tmap_v, sm, kStageV, cid, ncl, n_items, abort);
+                role_releaser(p, sm, cid, ncl, n_items, abort);
         }
-    } else if (warp == 5) {
+    } else if (warp >= 5) {
         if (rank == 0) {
-            if ((threadIdx.x & 31) == 0) role_score_mma(p, sm, tmem, cid, ncl, n_items, abort);
-        } else {
+            if ((threadIdx.x & 31) == 0) role_score_mma(p, sm, tmem, (uint32_t)(warp - 5), cid, ncl, n_items, abort);
+        } else if (warp == 5) {
             role_accum_mma(p, sm, tmem, cid, ncl, n_items, abort);
+        } else if ((threadIdx.x & 31) == 0) {
+            role_p_loader(p, sm, cid, ncl, n_items, abort);
         }
     } else {
         if (rank == 0)
-            role_softmax(p, sm, tmem, cid, ncl, n_items, abort, any_words);
+            role_softmax(p, sm, tmem, cid, ncl, n_items, abort);
         else
             role_accum_epilogue(p, sm, tmem, cid, ncl, n_items, abort);
     }
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // neither CTA retires while its partner may still write into it
+    cluster_sync_all();  // neither CTA retires while its partner may still arrive on it
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

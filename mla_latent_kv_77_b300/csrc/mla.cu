@@ -18,7 +18,6 @@ namespace mla {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxClusters = 160;     // workspace is sized for at most this many CTA pairs
 constexpr int kMaxRows = 65536;       // batch * q_len limit of the planner
 constexpr int kMaxQLen = 64;
 
@@ -59,7 +58,7 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
                 return MLA_ERR_CUDA;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
-            cfg.blockDim = dim3(192, 1, 1);
+            cfg.blockDim = dim3(kDecodeThreads, 1, 1);
             cfg.dynamicSmemBytes = kDecodeSmem;
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
@@ -123,7 +122,7 @@ bool tmap_pool_pages(CUtensorMap *m, const void *pool, uint64_t num_pages, uint3
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t hdr, items, info, part_lse, part_o, total;
+    size_t hdr, items, info, ring, part_lse, part_o, total;
     int max_items, max_slots;
 };
 
@@ -142,6 +141,8 @@ bool ws_layout(int batch, int q_len, int num_splits, WsLayout *w) {
     off = align_up(off + sizeof(Item) * (size_t)mi, 256);
     w->info = off;
     off = align_up(off + sizeof(BtInfo) * (size_t)n_bt, 256);
+    w->ring = off;  // P messages between the two CTAs of each pair
+    off = align_up(off + (size_t)kMaxClusters * kRing * kMsgBytes, 256);
     w->part_lse = off;
     off = align_up(off + sizeof(float) * kHeads * (size_t)mi, 256);
     w->part_o = off;
@@ -284,7 +285,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
 
     CUtensorMap tmap_s, tmap_v;
     if (!tmap_pool_pages(&tmap_s, kv_pool, (uint64_t)num_pages, kBoxesS) ||
-        !tmap_pool_pages(&tmap_v, kv_pool, (uint64_t)num_pages, kBoxesV))
+        !tmap_pool_pages(&tmap_v, kv_pool, (uint64_t)num_pages, kBoxesV / 2))
         return MLA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -308,6 +309,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     p.items = items;
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
     p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+    p.ring = ws + w.ring;
     p.B = batch;
     p.Tq = q_len;
     p.causal = causal ? 1 : 0;
@@ -317,7 +319,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * info->clusters, 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(kDecodeThreads, 1, 1);
     cfg.dynamicSmemBytes = kDecodeSmem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];

@@ -55,11 +55,17 @@ def test_static_scratch_refuses_requests_larger_than_the_array():
     bt, sl = case.block_table.cuda(), case.seq_lens.cuda()
     o = torch.empty(case.B, 1, 128, 512, dtype=torch.bfloat16, device="cuda")
     l = torch.empty(case.B, 1, 128, dtype=torch.float32, device="cuda")
-    # 96 queries need a little more than the 64 MiB array: refused before anything runs
-    big = workloads.make_case("static_big96", [64] * 96, seed=34)
+    # the smallest batch whose workspace exceeds the array (144 queries with the automatic
+    # plan) is refused before anything runs
+    limit = 64 << 20  # MLA_STATIC_SCRATCH_BYTES
+    n_big = 1
+    while mla.decode_workspace_size(n_big, 1, 0) <= limit:
+        n_big += 1
+    assert mla.decode_workspace_size(n_big - 1, 1, 0) <= limit < mla.decode_workspace_size(n_big, 1, 0)
+    big = workloads.make_case("static_big", [64] * n_big, seed=34)
     st = _static_call(big.q_abs.cuda(), big.pool.cuda(), big.block_table.cuda(), big.seq_lens.cuda(), big, 0,
-                      torch.empty(96, 1, 128, 512, dtype=torch.bfloat16, device="cuda"),
-                      torch.empty(96, 1, 128, dtype=torch.float32, device="cuda"))
+                      torch.empty(n_big, 1, 128, 512, dtype=torch.bfloat16, device="cuda"),
+                      torch.empty(n_big, 1, 128, dtype=torch.float32, device="cuda"))
     assert st == mla.Status.WORKSPACE
     # forced splits push a small batch over the limit too
     assert _static_call(q, pool, bt, sl, case, 4000, o, l) == mla.Status.WORKSPACE
