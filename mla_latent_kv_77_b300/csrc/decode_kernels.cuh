@@ -47,12 +47,13 @@ constexpr int kBoxesV = kDc / 64;    // 8 blocks per page for the value side (c 
 constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page
 constexpr uint32_t kStageV = kBoxesV / 2 * kBoxBytes;  // 32768: half of a page's latent columns
 constexpr int kStagesS = 3;          // score CTA page stages
-constexpr int kStagesV = 4;          // accumulate CTA half-page stages (two per page)
-constexpr int kPBufs = 4;            // accumulate CTA: P messages held in shared memory
+constexpr int kStagesV = 5;          // accumulate CTA half-page stages (two per page)
+constexpr int kPBufs = 3;            // accumulate CTA: P messages held in shared memory
 constexpr int kRing = 16;            // P messages in flight through global memory, per CTA pair
 constexpr int kBatch = 4;            // messages published together (one cluster-scope release each)
+constexpr int kShippers = 1;         // threads publishing batches, round robin
 constexpr int kRingBatches = kRing / kBatch;
-constexpr int kPrefetch = 6;         // pages prefetched into L2 ahead of the page being loaded
+constexpr int kPrefetch = 8;         // pages prefetched into L2 ahead of the page being loaded
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
 constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one ring slot in global memory
@@ -60,8 +61,10 @@ constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (fact
 constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns
-constexpr uint32_t kTmemS = 0;       // score CTA: the page's two partial S tiles at 0 and 64
-constexpr uint32_t kTmemQ = 128;     // score CTA: Q (bf16 pairs) at 128 .. 415
+constexpr int kIssuers = 3;          // score CTA MMA issuers, one partial S tile each
+constexpr int kBlocksPerIssuer = kBoxesS / kIssuers;  // 3 column blocks = 12 MMAs each
+constexpr uint32_t kTmemS = 0;       // score CTA: the page's three partial S tiles at 0, 64, 128
+constexpr uint32_t kTmemQ = 64 * kIssuers;  // score CTA: Q (bf16 pairs) at 192 .. 479
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory (offsets from a 1024-aligned base).  Score CTA: page stages at 0.
@@ -77,7 +80,7 @@ constexpr int kStagesMax = kStagesS > kStagesV ? kStagesS : kStagesV;
 constexpr int kBarFull = 0;                          // page stages (score) / half-page stages (accumulate)
 constexpr int kBarEmpty = kBarFull + kStagesMax;
 constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: partial S tile written (one per issuer)
-constexpr int kBarSEmpty = kBarSFull + 2;            // score: both partial tiles read by the softmax warps
+constexpr int kBarSEmpty = kBarSFull + kIssuers;     // score: all partial tiles read by the softmax warps
 constexpr int kBarQReady = kBarSEmpty + 1;           // score: the item's Q is in TMEM
 constexpr int kBarPFree = kBarQReady + 1;            // score: ring slot consumed (partner arrives)
 constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a batch of ring slots written (partner arrives)
@@ -86,11 +89,20 @@ constexpr int kBarPFull = kBarPStaged + kRing;       // accumulate: P buffer lan
 constexpr int kBarPBufFree = kBarPFull + kPBufs;     // accumulate: P buffer used by the MMAs and the releaser
 constexpr int kBarMmaEvt = kBarPBufFree + kPBufs;    // accumulate: event for the epilogue warps
 constexpr int kBarCorrEvt = kBarMmaEvt + 1;          // accumulate: event served
-constexpr int kNumBars = kBarCorrEvt + 1;
+constexpr int kBarXMax = kBarCorrEvt + 1;            // score: row-max swap, [quadrant][page parity]
+constexpr int kBarXSum = kBarXMax + 8;               // score: row-sum swap, [quadrant]
+constexpr int kNumBars = kBarXSum + 4;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kDecodeSmem = kOffAbort + 16 + 1024;  // + slack to align the base
-constexpr int kDecodeThreads = 256;  // 4 softmax/epilogue warps, producer, 2 MMA/loader warps, shipper/releaser
+constexpr uint32_t kOffXMax = (kOffAbort + 4 + 15u) & ~15u;   // score: row-max exchange [2][2][128] f32
+constexpr uint32_t kOffXSum = kOffXMax + 2 * 2 * kHeads * 4;  // score: row-sum exchange [2][128] f32
+constexpr uint32_t kDecodeSmem = kOffXSum + 2 * kHeads * 4 + 1024;  // + slack to align the base
+// warps: 0-7 softmax (score) / epilogue (accumulate), 8 page producer, 9-11 the three score
+// MMA issuers (score) / PV MMA, P loader, releaser (accumulate), 12 shipper (score)
+constexpr int kDecodeThreads = (12 + kShippers) * 32;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpShipper = 12;
+static_assert(kDecodeSmem <= 227u * 1024u, "decode kernel shared memory exceeds the per-CTA limit");
+static_assert(kTmemQ + 32u * kBoxesS <= kTmemCols, "score CTA tensor memory overflow");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);    // A = Q (TMEM), B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A = P K-major, B = V MN-major
@@ -126,6 +138,7 @@ struct DecodeParams {
     float *part_o;                // [slots, 128, 512]
     float *part_lse;              // [slots, 128]
     uint8_t *ring;                // [clusters, kRing, kMsgBytes] P messages
+    const uint8_t *pool;          // [num_pages, 64, 576] bf16 (for L2 prefetches)
     int B, Tq, causal, num_pages, max_pages;
     float sl2;                    // scale * log2(e)
 };
@@ -193,16 +206,24 @@ __device__ __forceinline__ int block_excl_scan(int v, int *tmp /*[32]*/, int *to
     return warp_off + x - v;
 }
 
+constexpr int kPlanSmemBt = 2048;  // queries planned in shared memory; larger batches use workspace scratch
+
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int max_pages,
             int n_clusters, int num_splits, PlanHeader *hdr, Item *items, BtInfo *info,
-            int max_items, int max_slots) {
+            int *scratch /* 4 * B * Tq ints, used when B * Tq > kPlanSmemBt */, int max_items, int max_slots) {
+    grid_launch_dependents();  // the decode kernel may start its prologue while the plan is made
     __shared__ int s_tmp[32];
     __shared__ int s_key[kPlanThreads];
     __shared__ int s_ord[kPlanThreads];
+    __shared__ int s_arr[4 * kPlanSmemBt];
     const int tid = threadIdx.x;
     const int n_bt = B * Tq;
     const int per = (n_bt + kPlanThreads - 1) / kPlanThreads;
+    int *const base = n_bt <= kPlanSmemBt ? s_arr : scratch;
+    const int stride = n_bt <= kPlanSmemBt ? kPlanSmemBt : n_bt;
+    int *const tiles = base, *const splits = base + stride, *const slot_base = base + 2 * stride,
+              *const item_off = base + 3 * stride;
 
     // 1. tiles per query, total work
     int w_local = 0;
@@ -215,7 +236,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
         }
         int n = visible_tokens(L, Tq, t, causal);
         int T = (n + kPage - 1) / kPage;
-        info[bt].tiles = T;
+        tiles[bt] = T;
         w_local += T;
     }
     int W_total;
@@ -224,7 +245,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
 
     // 2. split counts
     for (int bt = tid * per; bt < min(n_bt, (tid + 1) * per); ++bt) {
-        int T = info[bt].tiles;
+        int T = tiles[bt];
         int s = 1;
         int cap = T / kMinChunkTiles > 1 ? T / kMinChunkTiles : 1;
         if (num_splits > 0) {
@@ -238,7 +259,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
             }
             s = s < 1 ? 1 : (s > cap ? cap : s);
         }
-        info[bt].splits = s;
+        splits[bt] = s;
     }
     __syncthreads();
 
@@ -247,7 +268,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
     if (sorted) {
         int key = -1;
         if (tid < n_bt) {
-            int T = info[tid].tiles, s = info[tid].splits;
+            int T = tiles[tid], s = splits[tid];
             key = (T + s - 1) / s;
         }
         s_key[tid] = key;
@@ -267,37 +288,39 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
     int items_local = 0, slots_local = 0;
     for (int k = tid * per; k < min(n_bt, (tid + 1) * per); ++k) {
         int bt = sorted ? s_ord[k] : k;
-        items_local += info[bt].splits;
-        slots_local += info[k].splits > 1 ? info[k].splits : 0;
+        items_local += splits[bt];
+        slots_local += splits[k] > 1 ? splits[k] : 0;
     }
     int n_items, n_slots;
-    int item_off = block_excl_scan(items_local, s_tmp, &n_items);
-    int slot_off = block_excl_scan(slots_local, s_tmp, &n_slots);
+    int ioff = block_excl_scan(items_local, s_tmp, &n_items);
+    int soff = block_excl_scan(slots_local, s_tmp, &n_slots);
     const bool overflow = n_items > max_items || n_slots > max_slots;
     for (int k = tid * per; k < min(n_bt, (tid + 1) * per); ++k) {
         int bt = sorted ? s_ord[k] : k;
-        info[bt].item_off = item_off;
-        item_off += info[bt].splits;
-        int s2 = info[k].splits;
-        info[k].slot_base = s2 > 1 ? slot_off : -1;
-        slot_off += s2 > 1 ? s2 : 0;
+        item_off[bt] = ioff;
+        ioff += splits[bt];
+        int s2 = splits[k];
+        slot_base[k] = s2 > 1 ? soff : -1;
+        soff += s2 > 1 ? s2 : 0;
     }
     __syncthreads();
 
-    // 5. items (on overflow nothing is scheduled and nothing is combined)
-    if (overflow) {
-        for (int bt = tid * per; bt < min(n_bt, (tid + 1) * per); ++bt) info[bt].splits = 0;
-    } else {
-        for (int bt = tid * per; bt < min(n_bt, (tid + 1) * per); ++bt) {
-            BtInfo in = info[bt];
-            for (int j = 0; j < in.splits; ++j) {
-                Item it;
-                it.bt = bt;
-                it.tb = (int)(((long long)in.tiles * j) / in.splits);
-                it.te = (int)(((long long)in.tiles * (j + 1)) / in.splits);
-                it.slot = in.splits > 1 ? in.slot_base + j : -1;
-                items[in.item_off + j] = it;
-            }
+    // 5. items and the per-query info the combine kernel reads (on overflow nothing is
+    //    scheduled and nothing is combined)
+    for (int bt = tid * per; bt < min(n_bt, (tid + 1) * per); ++bt) {
+        BtInfo in;
+        in.splits = overflow ? 0 : splits[bt];
+        in.slot_base = slot_base[bt];
+        in.tiles = tiles[bt];
+        in.item_off = item_off[bt];
+        info[bt] = in;
+        for (int j = 0; j < in.splits; ++j) {
+            Item it;
+            it.bt = bt;
+            it.tb = (int)(((long long)in.tiles * j) / in.splits);
+            it.te = (int)(((long long)in.tiles * (j + 1)) / in.splits);
+            it.slot = in.splits > 1 ? in.slot_base + j : -1;
+            items[in.item_off + j] = it;
         }
     }
     if (tid == 0) {
@@ -321,25 +344,56 @@ struct Smem {
     __device__ __forceinline__ uint32_t evt() const { return base + kOffEvt; }
 };
 
+// L2 eviction policies.  Every page is read twice, by the score CTA and microseconds later by
+// its partner: the first read asks L2 to keep the lines (evict_last), the second lets them go
+// (evict_first).  The P ring is rewritten in place and should never leave L2 (evict_last).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void *tmap, int32_t x, int32_t y, int32_t z,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
         : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y), "r"(z)
+                 "r"(x), "r"(y), "r"(z), "l"(pol)
                  : "memory");
 }
 // global -> shared::cta bulk copy, completion counted on a local barrier
-__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+// One warp asks L2 for a whole page (576 lines of 128 bytes), to be kept until its second
+// read; plain per-lane prefetches leave the TMA unit to the loads themselves.
+__device__ __forceinline__ void prefetch_page_l2(const uint8_t *page, int lane) {
+#pragma unroll
+    for (int k = 0; k < kStageS / 128 / 32; ++k)
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(page + (size_t)(k * 32 + lane) * 128) : "memory");
+}
+__device__ __forceinline__ void st_global_v4_hint(void *dst, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
                  : "memory");
+}
+__device__ __forceinline__ void st_global_f32_hint(void *dst, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(pol) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 // arrive on a barrier of another CTA with no ordering of this thread's memory operations
@@ -365,9 +419,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
-// Every lane waits; if any lane of the warp gave up, the whole warp gives up.
-#define MLA_WAIT_WARP(expr) \
-    if (__any_sync(0xffffffffu, !(expr))) return
+// Waits of warps that run warp-collective instructions: every lane waits (keeping the warp
+// converged, which measured much faster here than one lane waiting and broadcasting), and if
+// any lane gave up, the whole warp gives up together.
+#define MLA_WAIT_WARP(bar_, par_, ab_) \
+    if (__any_sync(0xffffffffu, !mbar_wait(bar_, par_, ab_))) return
 
 // Page producer (a whole warp; lane 0 issues).  The tensor map views the pool as (64 columns,
 // rows, column blocks) with strides (2 B, 1152 B, 128 B), so one box lands in shared memory as
@@ -381,6 +437,8 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
                                               uint32_t stage_bytes, bool prefetch, int cid, int ncl, int n_items,
                                               volatile int *abort) {
     const int lane = threadIdx.x & 31;
+    // the score CTA's read is a page's first: keep it for the partner; the partner's is its last
+    const uint64_t pol = prefetch ? l2_policy_evict_last() : l2_policy_evict_first();
     uint32_t g = 0;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
@@ -390,9 +448,8 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
         int nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
         int chunk = it.tb;
         if (prefetch) {  // the item's first pages
-            const int pf = it.tb + (lane < kPrefetch ? lane : 0);
-            const int pg = __shfl_sync(0xffffffffu, cur, pf - it.tb);
-            if (lane < kPrefetch && pf < it.te) tma_prefetch_l2_3d(tmap, 0, pg * kPage, 0);
+            for (int k = 0; k < kPrefetch && it.tb + k < it.te; ++k)
+                prefetch_page_l2(p.pool + (size_t)__shfl_sync(0xffffffffu, cur, k) * kStageS, lane);
         }
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             if (tile - chunk == 32) {
@@ -411,11 +468,11 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
                 if (lane == 0) {
                     mbar_arrive_expect_tx(sm.bar(kBarFull + s), stage_bytes);
                     tma_load_3d(sm.stage(s, stage_bytes), tmap, 0, pg * kPage, hf * (kBoxesV / 2),
-                                sm.bar(kBarFull + s));
+                                sm.bar(kBarFull + s), pol);
                 }
                 __syncwarp();
             }
-            if (lane == 0 && prefetch && tile + kPrefetch < it.te) tma_prefetch_l2_3d(tmap, 0, fpg * kPage, 0);
+            if (prefetch && tile + kPrefetch < it.te) prefetch_page_l2(p.pool + (size_t)fpg * kStageS, lane);
         }
     }
     g *= kHalves;
@@ -425,14 +482,16 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
             if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
 }
 
-// Score CTA, MMA issuer `me` (0 or 1, one thread each).  Both issuers work on every page:
-// issuer 0 accumulates column blocks 0-4 of S = Q . K_tile^T into partial tile 0, issuer 1
-// blocks 5-8 into partial tile 1, each in fully unrolled steps with constant descriptor
-// offsets.  The page's stage is free once both have committed.
+// Score CTA, MMA issuer `me` (0..2, one thread each).  All issuers work on every page: issuer
+// `me` accumulates column blocks 3me .. 3me+2 of S = Q . K_tile^T into partial tile `me`, in
+// fully unrolled steps with constant descriptor offsets.  One thread issues N = 64 MMAs too
+// slowly to keep the tensor pipe busy; three splitting each page do, and a page then leaves
+// its stage as soon as the tensor pipe is done with it.  The stage is free once all three
+// have committed.
 __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, uint32_t me,
                                                int cid, int ncl, int n_items, volatile int *abort) {
-    constexpr int kSplit = 5;  // column blocks of issuer 0
     uint32_t g = 0, ic = 0;
+    const uint32_t bx0 = me * kBlocksPerIssuer;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
@@ -447,21 +506,12 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
             if (!mbar_wait(sm.bar(kBarSEmpty), (g & 1u) ^ 1u, abort)) return;
             tc_fence_after();
             const uint32_t d = tmem + kTmemS + me * 64u;
-            const uint64_t b0 = sdesc_sw128(sm.stage(s, kStageS), 16u, 1024u);
-            if (me == 0) {
+            const uint32_t a0 = tmem + kTmemQ + bx0 * 32u;
+            const uint64_t b0 = sdesc_sw128(sm.stage(s, kStageS) + bx0 * kBoxBytes, 16u, 1024u);
 #pragma unroll
-                for (int k = 0; k < 4 * kSplit; ++k) {
-                    const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
-                    mma_ts(d, tmem + kTmemQ + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4),
-                           kIdescS, k != 0);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4 * (kBoxesS - kSplit); ++k) {
-                    const uint32_t bx = kSplit + ((uint32_t)k >> 2), kk = (uint32_t)k & 3u;
-                    mma_ts(d, tmem + kTmemQ + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4),
-                           kIdescS, k != 0);
-                }
+            for (int k = 0; k < 4 * kBlocksPerIssuer; ++k) {
+                const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
+                mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS, k != 0);
             }
             mma_commit(sm.bar(kBarEmpty + s));
             mma_commit(sm.bar(kBarSFull + me));
@@ -469,80 +519,104 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
     }
 }
 
-// Score CTA, softmax warps (thread = head).  Per page: read S, online softmax with lazy
-// rescaling, write the P message (bf16 row in the UMMA K-major 128-byte-swizzle image,
-// the rescale factor, and 1/l on the item's last page) into the ring, then signal.
+// Score CTA, softmax warps.  Eight warps, two per sub-partition: warp w owns heads
+// 32(w%4) .. 32(w%4)+31 (its TMEM lane quadrant) and columns [32 hf, 32 hf + 32) of each page,
+// hf = w / 4.  The two threads of a head swap their row maxima through shared memory every
+// page (and their row sums on an item's last page), so both take identical rescale decisions.
+// Per page: add the partial S tiles, online softmax with lazy rescaling, write the half-row of
+// the P message (bf16 in the UMMA K-major 128-byte-swizzle image, the rescale factor, and 1/l on
+// the item's last page) into the ring, then signal the shipper.
 __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
                                              int ncl, int n_items, volatile int *abort) {
-    const int h = threadIdx.x;  // 0..127
-    const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
+    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2;
+    const int h = q4 * 32 + (threadIdx.x & 31);
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.sl2;
     const uint32_t row_off = (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u;
     uint8_t *const ring = p.ring + (size_t)cid * kRing * kMsgBytes;
-    uint32_t sc = 0;
+    const uint32_t xmax = sm.base + kOffXMax, xsum = sm.base + kOffXSum;
+    const uint64_t keep = l2_policy_evict_last();
+    uint32_t sc = 0, nsum = 0;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
         const ItemInfo it = load_item(p, i);
         if (it.te <= it.tb) {
-            p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
+            if (hf == 0) p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
             continue;
         }
-        // absorbed query of this head -> TMEM lane h (bf16 pairs, 288 columns)
+        // absorbed query of this head -> TMEM lane h (bf16 pairs, 288 columns; blocks 0-4 by the
+        // first half, 5-8 by the second).  The next block's loads are in flight while one block
+        // is stored, so the item start pays about one memory latency per two blocks.
         {
             const uint4 *q = reinterpret_cast<const uint4 *>(p.q_abs + ((size_t)it.bt * kHeads + h) * kD);
-#pragma unroll 1
-            for (int c = 0; c < kBoxesS; ++c) {
-                uint32_t v[32];
+            const int c0 = hf ? 5 : 0, c1 = hf ? kBoxesS : 5;
+            uint4 va[8], vb[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint4 x = __ldg(q + c * 8 + u);
-                    v[4 * u + 0] = x.x;
-                    v[4 * u + 1] = x.y;
-                    v[4 * u + 2] = x.z;
-                    v[4 * u + 3] = x.w;
+            for (int u = 0; u < 8; ++u) va[u] = __ldg(q + c0 * 8 + u);
+#pragma unroll 1
+            for (int c = c0; c < c1; c += 2) {
+                const bool has_b = c + 1 < c1, has_a2 = c + 2 < c1;
+                if (has_b) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) vb[u] = __ldg(q + (c + 1) * 8 + u);
                 }
-                tmem_st32(tmem + lane_off + kTmemQ + c * 32u, v);
+                tmem_st32(tmem + lane_off + kTmemQ + c * 32u, *reinterpret_cast<const uint32_t(*)[32]>(va));
+                if (has_a2) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) va[u] = __ldg(q + (c + 2) * 8 + u);
+                }
+                if (has_b) tmem_st32(tmem + lane_off + kTmemQ + (c + 1) * 32u, *reinterpret_cast<const uint32_t(*)[32]>(vb));
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarQReady));
         }
-        float m = 0.f, l = 0.f;
+        float m = 0.f, l = 0.f, lt = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
-            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarSFull + 0), sc & 1u, abort));
-            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarSFull + 1), sc & 1u, abort));
+#pragma unroll
+            for (int t = 0; t < kIssuers; ++t) MLA_WAIT_WARP(sm.bar(kBarSFull + t), sc & 1u, abort);
             tc_fence_after();
-            float s[64];
+            float s[32];
             {
-                uint32_t a[32], b[32];
+                uint32_t a[32], b[32], c3[32];
+                tmem_ld32(tmem + lane_off + kTmemS + 32u * hf, a);
+                tmem_ld32(tmem + lane_off + kTmemS + 64u + 32u * hf, b);
+                tmem_ld32(tmem + lane_off + kTmemS + 128u + 32u * hf, c3);
+                tmem_ld_wait();
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    tmem_ld32(tmem + lane_off + kTmemS + 32u * hf, a);
-                    tmem_ld32(tmem + lane_off + kTmemS + 64u + 32u * hf, b);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) s[32 * hf + c] = __uint_as_float(a[c]) + __uint_as_float(b[c]);
-                }
+                for (int c = 0; c < 32; ++c)
+                    s[c] = (__uint_as_float(a[c]) + __uint_as_float(b[c])) + __uint_as_float(c3[c]);
             }
             tc_fence_before();
             mbar_arrive(sm.bar(kBarSEmpty));
 
-            const int valid = min(kPage, it.n_vis - tile * kPage);
-            if (valid < kPage) {
+            const int valid = min(kPage, it.n_vis - tile * kPage) - 32 * hf;  // columns of this half
+            if (valid < 32) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                for (int c = 0; c < 32; ++c) s[c] = c < valid ? s[c] : -INFINITY;
             }
-            // row max as a tree (fmaxf is exact, so the order does not matter)
+            // row max: this half as a tree (fmaxf is exact, so the order does not matter), then
+            // the partner's half through shared memory (double-buffered by page parity)
             float mx4[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float a = s[16 * q4];
+            for (int g4 = 0; g4 < 4; ++g4) {
+                float a = s[8 * g4];
 #pragma unroll
-                for (int c = 1; c < 16; ++c) a = fmaxf(a, s[16 * q4 + c]);
-                mx4[q4] = a;
+                for (int c = 1; c < 8; ++c) a = fmaxf(a, s[8 * g4 + c]);
+                mx4[g4] = a;
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+            const float lmx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const uint32_t xb = xmax + (sc & 1u) * (2u * kHeads * 4u);
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(xb + (uint32_t)(hf * kHeads + h) * 4u), "f"(lmx) : "memory");
+            {  // both warps of the quadrant have written (a bounded wait, unlike a named barrier)
+                const uint32_t xbar = sm.bar(kBarXMax + 2 * q4 + (int)(sc & 1u));
+                mbar_arrive(xbar);
+                MLA_WAIT_WARP(xbar, (sc >> 1) & 1u, abort);
+            }
+            float omx;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(omx) : "r"(xb + (uint32_t)((1 - hf) * kHeads + h) * 4u) : "memory");
+            const float mx = fmaxf(lmx, omx) * sl2;
             const bool first = tile == it.tb;
             const bool last = tile == it.te - 1;
             float alpha = 1.f;
@@ -553,63 +627,80 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 l *= alpha;
                 m = mx;
             }
-            uint32_t pk[32];
+            uint32_t pk[16];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 16; ++c) {
                 const float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
                 const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
                 pk[c] = pack_bf16x2(a, b);
                 ls[c & 3] += a + b;  // the row sum uses the unrounded probabilities (exact lse)
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            if (last) {  // the whole row's sum, for 1/l and the lse
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + (uint32_t)(hf * kHeads + h) * 4u), "f"(l) : "memory");
+                const uint32_t sbar = sm.bar(kBarXSum + q4);
+                mbar_arrive(sbar);
+                MLA_WAIT_WARP(sbar, nsum & 1u, abort);
+                ++nsum;
+                float ol;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ol) : "r"(xsum + (uint32_t)((1 - hf) * kHeads + h) * 4u) : "memory");
+                lt = hf == 0 ? l + ol : ol + l;  // the same sum, in the same order, in both halves
+            }
 
             // the message, straight into its ring slot once the partner has taken the slot's
             // previous content (a plain signal: that copy completed before the partner
-            // arrived): P row in the UMMA K-major 128-byte-swizzle image, the rescale factor,
-            // and 1/l on the item's last page
+            // arrived): this half-row of P in the UMMA K-major 128-byte-swizzle image, the
+            // rescale factor, and 1/l on the item's last page
             const uint32_t rs = sc % kRing;
-            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarPFree + rs), ((sc / kRing) & 1u) ^ 1u, abort));
+            MLA_WAIT_WARP(sm.bar(kBarPFree + rs), ((sc / kRing) & 1u) ^ 1u, abort);
             uint8_t *msg = ring + (size_t)rs * kMsgBytes;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 *dst = reinterpret_cast<uint4 *>(msg + row_off + (uint32_t)((c ^ (h & 7)) * 16));
-                *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int u = 0; u < 4; ++u) {
+                const int c = 4 * hf + u;
+                st_global_v4_hint(msg + row_off + (uint32_t)((c ^ (h & 7)) * 16),
+                                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]), keep);
             }
-            reinterpret_cast<float *>(msg + kPBytes)[h] = alpha;
-            if (last) reinterpret_cast<float *>(msg + kPBytes)[kHeads + h] = 1.0f / l;
+            if (hf == 0) {
+                st_global_f32_hint(msg + kPBytes + 4u * h, alpha, keep);
+                if (last) st_global_f32_hint(msg + kPBytes + 4u * (kHeads + h), 1.0f / lt, keep);
+            }
             // local release; the shipper publishes the slot to the partner
             mbar_arrive(sm.bar(kBarPStaged + rs));
         }
-        const float lse = (m + __log2f(l)) * 0.69314718055994531f;
-        if (it.slot < 0)
-            p.lse[(size_t)it.bt * kHeads + h] = lse;
-        else
-            p.part_lse[(size_t)it.slot * kHeads + h] = lse;
+        if (hf == 0) {
+            const float lse = (m + __log2f(lt)) * 0.69314718055994531f;
+            if (it.slot < 0)
+                p.lse[(size_t)it.bt * kHeads + h] = lse;
+            else
+                p.part_lse[(size_t)it.slot * kHeads + h] = lse;
+        }
     }
 }
 
-// Score CTA, shipper (one thread): publishes the ring slots the softmax warps have written
-// to the partner, kBatch at a time, with one cluster-scope release per batch.  It acquires
-// the rows through the local barrier, and release/acquire chains are transitive, so the
-// partner's acquire sees every row.  Such a release waits for the rows' stores to complete
-// and costs about a microsecond here, too much to pay per message; and the compute warps
-// never touch a cluster-scope barrier.
+// Score CTA, shippers (one thread each, kShippers of them): publish the ring slots the
+// softmax warps have written to the partner, kBatch at a time, with one cluster-scope release
+// per batch; shipper j handles the batches b with b % kShippers == j.  A shipper acquires the
+// rows through the local barrier, and release/acquire chains are transitive, so the partner's
+// acquire sees every row.  Such a release waits for the rows' stores to complete and costs
+// about a microsecond here: batching and several shippers keep that off the page rate, and
+// the compute warps never touch a cluster-scope barrier.
 static_assert(kRing % kBatch == 0 && kRingBatches >= 3, "ring must hold at least three batches");
-__device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
-                                             volatile int *abort) {
+__device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, uint32_t me, int cid, int ncl,
+                                             int n_items, volatile int *abort) {
     uint32_t g = 0;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
         const ItemInfo it = load_item(p, i);
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
+            if ((g / kBatch) % kShippers != me) continue;
             if (!mbar_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
             if ((g + 1) % kBatch == 0)
                 mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
         }
     }
-    if (g % kBatch != 0)  // the last, partial batch
+    if (g % kBatch != 0 && (g / kBatch) % kShippers == me)  // the last, partial batch
         mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
 }
 
@@ -637,6 +728,7 @@ __device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem 
 __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
                                               volatile int *abort) {
     const uint8_t *ring = p.ring + (size_t)cid * kRing * kMsgBytes;
+    const uint64_t keep = l2_policy_evict_last();
     uint32_t g = 0;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
@@ -652,8 +744,8 @@ __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem 
             if (!mbar_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
             mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
             const uint8_t *msg = ring + (size_t)rs * kMsgBytes;
-            bulk_load_g2s(sm.pbuf(jp), msg, kPBytes, sm.bar(kBarPFull + jp));
-            bulk_load_g2s(sm.meta(jp), msg + kPBytes, kMetaBytes, sm.bar(kBarPFull + jp));
+            bulk_load_g2s(sm.pbuf(jp), msg, kPBytes, sm.bar(kBarPFull + jp), keep);
+            bulk_load_g2s(sm.meta(jp), msg + kPBytes, kMetaBytes, sm.bar(kBarPFull + jp), keep);
         }
     }
 }
@@ -759,12 +851,15 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
     if (pending_epilogue) warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort);
 }
 
-// Accumulate CTA, epilogue warps (thread = head): serve events -- rescale O rows, or
-// write the normalised output of the finished item.
+// Accumulate CTA, epilogue warps.  Eight warps: warp w owns heads 32(w%4) .. +31 (its TMEM
+// lane quadrant) and latent columns [256 hf, 256 hf + 256), hf = w / 4.  They serve events --
+// rescale their part of the O rows, or write the normalised output of the finished item.
 __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const Smem &sm, uint32_t tmem,
                                                     int cid, int ncl, int n_items, volatile int *abort) {
-    const int h = threadIdx.x;  // 0..127
-    const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
+    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2;
+    const int h = q4 * 32 + (threadIdx.x & 31);
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t col0 = 256u * hf;
     const uint32_t evt = sm.evt();
     uint32_t ev = 0;
     for (int r = 0;; ++r) {
@@ -772,12 +867,12 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
         if (i >= n_items) break;
         const ItemInfo it = load_item(p, i);
         if (it.te <= it.tb) {
-            uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc);
-            for (int c = 0; c < kDc * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
+            uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + col0);
+            for (int c = 0; c < 256 * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
             continue;
         }
         for (;;) {
-            MLA_WAIT_WARP(mbar_wait(sm.bar(kBarMmaEvt), ev & 1u, abort));
+            MLA_WAIT_WARP(sm.bar(kBarMmaEvt), ev & 1u, abort);
             ++ev;
             tc_fence_after();
             uint32_t type;
@@ -787,13 +882,13 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(alpha) : "r"(evt + 4u * h) : "memory");
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < kDc / 32; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + c * 32u, v);
+                        tmem_ld32(tmem + lane_off + col0 + c * 32u, v);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st32(tmem + lane_off + c * 32u, v);
+                        tmem_st32(tmem + lane_off + col0 + c * 32u, v);
                     }
                     tmem_st_wait();
                 }
@@ -804,23 +899,23 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
             float inv_l;
             asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv_l) : "r"(evt + 512u + 4u * h) : "memory");
 #pragma unroll 1
-            for (int c = 0; c < kDc / 32; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_off + c * 32u, v);
+                tmem_ld32(tmem + lane_off + col0 + c * 32u, v);
                 tmem_ld_wait();
                 if (it.slot < 0) {
-                    uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + c * 32);
+                    uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + col0 + c * 32);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv_l, __uint_as_float(v[8 * u + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv_l, __uint_as_float(v[8 * u + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv_l, __uint_as_float(v[8 * u + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv_l, __uint_as_float(v[8 * u + 7]) * inv_l);
-                        o[u] = w;
+                        uint4 q;
+                        q.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv_l, __uint_as_float(v[8 * u + 1]) * inv_l);
+                        q.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv_l, __uint_as_float(v[8 * u + 3]) * inv_l);
+                        q.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv_l, __uint_as_float(v[8 * u + 5]) * inv_l);
+                        q.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv_l, __uint_as_float(v[8 * u + 7]) * inv_l);
+                        o[u] = q;
                     }
                 } else {
-                    float4 *o = reinterpret_cast<float4 *>(p.part_o + ((size_t)it.slot * kHeads + h) * kDc + c * 32);
+                    float4 *o = reinterpret_cast<float4 *>(p.part_o + ((size_t)it.slot * kHeads + h) * kDc + col0 + c * 32);
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         o[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
@@ -834,10 +929,10 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
     }
 }
 
-// Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates), 256 threads:
-// warps 0-3 softmax (rank 0) / epilogue (rank 1), warp 4 page producer, warps 5-6 the two
-// score MMA issuers (rank 0) / the PV MMA warp and the P loader (rank 1), warp 7 the
-// message shipper (rank 0) / the ring-slot releaser (rank 1).
+// Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates), 13 warps:
+// 0-7 softmax (rank 0) / epilogue (rank 1), 8 page producer, 9-11 the three score MMA issuers
+// (rank 0) / the PV MMA warp, the P loader and the ring-slot releaser (rank 1), 12 the
+// message shipper (rank 0).
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_v,
               const DecodeParams p) {
@@ -855,66 +950,69 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesMax; ++s) {
             mbar_init(sm.bar(kBarFull + s), 1);
-            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? 2 : 1);  // score: both issuers commit
+            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? kIssuers : 1);  // score: every issuer commits
         }
-        for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
-        mbar_init(sm.bar(kBarSEmpty), 128);
-        mbar_init(sm.bar(kBarQReady), 128);
+        for (int j = 0; j < kIssuers; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
+        mbar_init(sm.bar(kBarSEmpty), 256);  // every softmax thread
+        mbar_init(sm.bar(kBarQReady), 256);
         for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPFree + j), 1);  // score CTA: the partner's releaser
         for (int j = 0; j < kRingBatches; ++j) mbar_init(sm.bar(kBarPReady + j), 1);  // accumulate CTA: the shipper
-        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPStaged + j), 128);  // score CTA: softmax threads
+        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPStaged + j), 256);  // score CTA: softmax threads
         for (int j = 0; j < kPBufs; ++j) {
             mbar_init(sm.bar(kBarPFull + j), 1);     // accumulate CTA: armed by the P loader
             mbar_init(sm.bar(kBarPBufFree + j), 2);  // accumulate CTA: MMA commit + releaser
         }
         mbar_init(sm.bar(kBarMmaEvt), 2);            // MMA warp arrive + MMA commit
-        mbar_init(sm.bar(kBarCorrEvt), 128);
+        mbar_init(sm.bar(kBarCorrEvt), 256);  // every epilogue thread
+        for (int j = 0; j < 12; ++j) mbar_init(sm.bar(kBarXMax + j), 64);  // the two warps of a quadrant
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(sm.base + kOffTmemPtr, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && (threadIdx.x & 31) == 0) tma_prefetch_desc(rank == 0 ? &tmap_s : &tmap_v);
+    if (warp == kWarpProducer && (threadIdx.x & 31) == 0) tma_prefetch_desc(rank == 0 ? &tmap_s : &tmap_v);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // the partner's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of the plan kernel: everything above overlapped it;
+    // the plan's results are read only after it has completed
+    grid_dependency_wait();
+    grid_launch_dependents();  // let the combine kernel's blocks get resident early
     const int n_items = p.hdr->n_items;
 
-    if (warp == 4) {
-        if (rank == 0)
-            role_producer<kStagesS, 1>(p, &tmap_s, sm, kStageS, true, cid, ncl, n_items, abort);
-        else
-            role_producer<kStagesV, 2>(p, &tmap_v, sm, kStageV, false, cid, ncl, n_items, abort);
-    } else if (warp == 7) {
-        if ((threadIdx.x & 31) == 0) {
-            if (rank == 0)
-                role_shipper(p, sm, cid, ncl, n_items, abort);
-            else
-                role_releaser(p, sm, cid, ncl, n_items, abort);
-        }
-    } else if (warp >= 5) {
-        if (rank == 0) {
-            if ((threadIdx.x & 31) == 0) role_score_mma(p, sm, tmem, (uint32_t)(warp - 5), cid, ncl, n_items, abort);
-        } else if (warp == 5) {
-            role_accum_mma(p, sm, tmem, cid, ncl, n_items, abort);
-        } else if ((threadIdx.x & 31) == 0) {
-            role_p_loader(p, sm, cid, ncl, n_items, abort);
-        }
-    } else {
+    const bool lane0 = (threadIdx.x & 31) == 0;
+    if (warp < 8) {
         if (rank == 0)
             role_softmax(p, sm, tmem, cid, ncl, n_items, abort);
         else
             role_accum_epilogue(p, sm, tmem, cid, ncl, n_items, abort);
+    } else if (warp == kWarpProducer) {
+        if (rank == 0)
+            role_producer<kStagesS, 1>(p, &tmap_s, sm, kStageS, true, cid, ncl, n_items, abort);
+        else
+            role_producer<kStagesV, 2>(p, &tmap_v, sm, kStageV, false, cid, ncl, n_items, abort);
+    } else if (warp < kWarpMma + kIssuers) {
+        if (rank == 0) {
+            if (lane0) role_score_mma(p, sm, tmem, (uint32_t)(warp - kWarpMma), cid, ncl, n_items, abort);
+        } else if (warp == kWarpMma) {
+            role_accum_mma(p, sm, tmem, cid, ncl, n_items, abort);
+        } else if (warp == kWarpMma + 1) {
+            if (lane0) role_p_loader(p, sm, cid, ncl, n_items, abort);
+        } else {
+            if (lane0) role_releaser(p, sm, cid, ncl, n_items, abort);
+        }
+    } else if (warp >= kWarpShipper) {
+        if (rank == 0 && lane0) role_shipper(p, sm, (uint32_t)(warp - kWarpShipper), cid, ncl, n_items, abort);
     }
 
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // neither CTA retires while its partner may still arrive on it
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -963,6 +1061,7 @@ __device__ __forceinline__ void combine_row(const float *o_base, size_t o_stride
 __global__ void __launch_bounds__(128)
 combine_kernel(const BtInfo *__restrict__ info, const float *__restrict__ part_o,
                const float *__restrict__ part_lse, __nv_bfloat16 *__restrict__ o_lat, float *__restrict__ lse) {
+    grid_dependency_wait();  // launched as a programmatic dependent of the decode kernel
     const int bt = blockIdx.x;
     const BtInfo in = info[bt];
     if (in.splits <= 1) return;

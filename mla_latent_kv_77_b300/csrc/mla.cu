@@ -119,10 +119,45 @@ bool tmap_pool_pages(CUtensorMap *m, const void *pool, uint64_t num_pages, uint3
     return r == CUDA_SUCCESS;
 }
 
+// Pool tensor maps are encoded once per (device, pool, pages, blocks) and reused: a decode
+// step of a serving loop sees the same pool every call.
+struct PoolMapEntry {
+    int dev;
+    const void *pool;
+    uint64_t num_pages;
+    uint32_t blocks;
+    CUtensorMap map;
+};
+constexpr int kPoolMapCache = 16;
+PoolMapEntry g_pool_maps[kPoolMapCache];
+int g_pool_maps_n = 0, g_pool_maps_next = 0;
+std::mutex g_map_mu;
+
+bool pool_map_cached(CUtensorMap *m, int dev, const void *pool, uint64_t num_pages, uint32_t blocks) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_pool_maps_n; ++i) {
+        const PoolMapEntry &e = g_pool_maps[i];
+        if (e.dev == dev && e.pool == pool && e.num_pages == num_pages && e.blocks == blocks) {
+            *m = e.map;
+            return true;
+        }
+    }
+    if (!tmap_pool_pages(m, pool, num_pages, blocks)) return false;
+    PoolMapEntry &e = g_pool_maps[g_pool_maps_next];
+    e.dev = dev;
+    e.pool = pool;
+    e.num_pages = num_pages;
+    e.blocks = blocks;
+    e.map = *m;
+    g_pool_maps_next = (g_pool_maps_next + 1) % kPoolMapCache;
+    if (g_pool_maps_n < kPoolMapCache) ++g_pool_maps_n;
+    return true;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t hdr, items, info, ring, part_lse, part_o, total;
+    size_t hdr, items, info, scratch, ring, part_lse, part_o, total;
     int max_items, max_slots;
 };
 
@@ -141,6 +176,8 @@ bool ws_layout(int batch, int q_len, int num_splits, WsLayout *w) {
     off = align_up(off + sizeof(Item) * (size_t)mi, 256);
     w->info = off;
     off = align_up(off + sizeof(BtInfo) * (size_t)n_bt, 256);
+    w->scratch = off;  // the planner's per-query arrays, for batches too large for its shared memory
+    off = align_up(off + (n_bt > kPlanSmemBt ? sizeof(int) * 4 * (size_t)n_bt : 0), 256);
     w->ring = off;  // P messages between the two CTAs of each pair
     off = align_up(off + (size_t)kMaxClusters * kRing * kMsgBytes, 256);
     w->part_lse = off;
@@ -284,8 +321,8 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     if (st != MLA_OK) return st;
 
     CUtensorMap tmap_s, tmap_v;
-    if (!tmap_pool_pages(&tmap_s, kv_pool, (uint64_t)num_pages, kBoxesS) ||
-        !tmap_pool_pages(&tmap_v, kv_pool, (uint64_t)num_pages, kBoxesV / 2))
+    if (!pool_map_cached(&tmap_s, dev, kv_pool, (uint64_t)num_pages, kBoxesS) ||
+        !pool_map_cached(&tmap_v, dev, kv_pool, (uint64_t)num_pages, kBoxesV / 2))
         return MLA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -296,7 +333,8 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     cudaStream_t s = (cudaStream_t)stream;
 
     plan_kernel<<<1, kPlanThreads, 0, s>>>(seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
-                                           num_splits, hdr, items, bt_info, w.max_items, w.max_slots);
+                                           num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch),
+                                           w.max_items, w.max_slots);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
     DecodeParams p;
@@ -310,6 +348,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
     p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
     p.ring = ws + w.ring;
+    p.pool = static_cast<const uint8_t *>(kv_pool);
     p.B = batch;
     p.Tq = q_len;
     p.causal = causal ? 1 : 0;
@@ -322,19 +361,33 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     cfg.blockDim = dim3(kDecodeThreads, 1, 1);
     cfg.dynamicSmemBytes = kDecodeSmem;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    // the decode and combine kernels are programmatic dependents of their predecessors: their
+    // launch and prologue overlap the predecessor, and they wait for its results on the device
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, p) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
-    combine_kernel<<<dim3(n_bt, kHeads / 8), 128, 0, s>>>(bt_info, p.part_o, p.part_lse, p.o_lat, lse);
-    return launch_error();
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(n_bt, kHeads / 8, 1);
+    ccfg.blockDim = dim3(128, 1, 1);
+    ccfg.stream = s;
+    ccfg.attrs = &at[1];
+    ccfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&ccfg, combine_kernel, (const BtInfo *)bt_info, (const float *)p.part_o,
+                           (const float *)p.part_lse, p.o_lat, lse) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
 }
 
 mla_status_t mla_decode_static_scratch(const void *q_abs, const void *kv_pool, const int32_t *block_table,

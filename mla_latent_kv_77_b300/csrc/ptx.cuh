@@ -122,6 +122,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch
+// ----------------------------------------------------------------------------
+// Block until the grids this one depends on have completed and their writes are visible
+// (a no-op when the kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream, if launched as a programmatic dependent, to start.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // Proxy fences / named barriers
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void fence_proxy_async_smem() {
