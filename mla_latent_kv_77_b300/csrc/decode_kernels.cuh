@@ -95,8 +95,8 @@ constexpr int kNumBars = kBarXSum + 4;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kOffXMax = (kOffAbort + 4 + 15u) & ~15u;   // score: row-max exchange [2][2][128] f32
-constexpr uint32_t kOffXSum = kOffXMax + 2 * 2 * kHeads * 4;  // score: row-sum exchange [2][128] f32
-constexpr uint32_t kDecodeSmem = kOffXSum + 2 * kHeads * 4 + 1024;  // + slack to align the base
+constexpr uint32_t kOffXSum = kOffXMax + 2 * 2 * kHeads * 4;  // score: row-sum exchange [2 sums][2][128] f32
+constexpr uint32_t kDecodeSmem = kOffXSum + 2 * 2 * kHeads * 4 + 1024;  // + slack to align the base
 // warps: 0-7 softmax (score) / epilogue (accumulate), 8 page producer, 9-11 the three score
 // MMA issuers (score) / PV MMA, P loader, releaser (accumulate), 12 shipper (score)
 constexpr int kDecodeThreads = (12 + kShippers) * 32;
@@ -572,7 +572,10 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             tc_fence_before();
             mbar_arrive(sm.bar(kBarQReady));
         }
-        float m = 0.f, l = 0.f, lt = 0.f;
+        // l: the row sum of the unrounded probabilities (for the lse); lr: the sum of the bf16
+        // probabilities the PV product actually uses, which normalises O -- numerator and
+        // denominator then carry the same rounding, which matters when a few tokens dominate
+        float m = 0.f, l = 0.f, lr = 0.f, lt = 0.f, lrt = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
 #pragma unroll
             for (int t = 0; t < kIssuers; ++t) MLA_WAIT_WARP(sm.bar(kBarSFull + t), sc & 1u, abort);
@@ -625,27 +628,35 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             } else if (mx > m + kTau) {
                 alpha = ex2_approx(m - mx);
                 l *= alpha;
+                lr *= alpha;
                 m = mx;
             }
             uint32_t pk[16];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            float ls[4] = {0.f, 0.f, 0.f, 0.f}, lsr[2] = {0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
                 const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
                 pk[c] = pack_bf16x2(a, b);
-                ls[c & 3] += a + b;  // the row sum uses the unrounded probabilities (exact lse)
+                ls[c & 3] += a + b;
+                lsr[c & 1] += bf16lo_to_f32(pk[c]) + bf16hi_to_f32(pk[c]);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (last) {  // the whole row's sum, for 1/l and the lse
+            lr += lsr[0] + lsr[1];
+            if (last) {  // the whole row's sums, for 1/l and the lse
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + (uint32_t)(hf * kHeads + h) * 4u), "f"(l) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + (uint32_t)((2 + hf) * kHeads + h) * 4u), "f"(lr)
+                             : "memory");
                 const uint32_t sbar = sm.bar(kBarXSum + q4);
                 mbar_arrive(sbar);
                 MLA_WAIT_WARP(sbar, nsum & 1u, abort);
                 ++nsum;
-                float ol;
+                float ol, olr;
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ol) : "r"(xsum + (uint32_t)((1 - hf) * kHeads + h) * 4u) : "memory");
-                lt = hf == 0 ? l + ol : ol + l;  // the same sum, in the same order, in both halves
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(olr) : "r"(xsum + (uint32_t)((3 - hf) * kHeads + h) * 4u)
+                             : "memory");
+                lt = hf == 0 ? l + ol : ol + l;  // the same sums, in the same order, in both halves
+                lrt = hf == 0 ? lr + olr : olr + lr;
             }
 
             // the message, straight into its ring slot once the partner has taken the slot's
@@ -663,7 +674,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             }
             if (hf == 0) {
                 st_global_f32_hint(msg + kPBytes + 4u * h, alpha, keep);
-                if (last) st_global_f32_hint(msg + kPBytes + 4u * (kHeads + h), 1.0f / lt, keep);
+                if (last) st_global_f32_hint(msg + kPBytes + 4u * (kHeads + h), 1.0f / lrt, keep);
             }
             // local release; the shipper publishes the slot to the partner
             mbar_arrive(sm.bar(kBarPStaged + rs));
