@@ -6,22 +6,26 @@
 // stays in latent space, o = sum_j softmax(s)_j c_j (W^UV is applied later).
 //
 // B300 design: one cluster of two CTAs (two SMs) per work item.
-//   CTA rank 0, the "score" CTA: holds the 128x576 absorbed query of the item in
-//     tensor memory (A operand, 288 columns), streams the 64-token pages with one
-//     3-D TMA per page into a 3-stage ring (plus L2 prefetches further ahead),
+//   CTA rank 0, the "score" CTA: holds the 128x576 absorbed query of the item as
+//     the MMA A operand (content part in tensor memory, RoPE part in shared
+//     memory), streams the 64-token pages with one
+//     3-D TMA per page into a 2-stage ring (L2 is asked to keep each page for
+//     the partner's second read),
 //     and computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05.
-//     Two MMA warps split each page's K range (column blocks 0-4 and 5-8) into
-//     two partial S tiles: one thread cannot issue N = 64 MMAs fast enough to
-//     keep the tensor pipe busy, two can, and a page then leaves its stage as
-//     soon as the tensor pipe is done with it.  Four softmax warps (thread =
-//     head) add the partials, run the online softmax with lazy rescaling and
-//     write P (bf16, 128 x 64) plus per-head factors straight from registers
-//     into a ring of messages in global memory (it stays in L2).
+//     Two MMA warps split each page's K range (column blocks 0-3, and 4-7 plus
+//     the RoPE block 8) into two partial S tiles -- one thread cannot issue
+//     N = 64 MMAs fast enough to keep the tensor pipe busy, two can -- and the
+//     partial tiles are double-buffered, so the next page's MMAs run while the
+//     softmax warps read this one's.  That fits because the query's content part
+//     (256 columns) sits in TMEM and its RoPE part in shared memory.  Eight
+//     softmax warps add the partials, run the online softmax with lazy
+//     rescaling and write P (bf16, 128 x 64) plus per-head factors straight from
+//     registers into a ring of messages in global memory (it stays in L2).
 //   CTA rank 1, the "accumulate" CTA: holds O = 128 heads x 512 latent fp32, i.e.
 //     all 512 TMEM columns, streams the same pages' 512 latent columns (L2 hits:
 //     the score CTA has just pulled them from HBM), bulk-copies each P message
 //     into shared memory, and runs O += P V (M = 128, N = 256 x 2, K = 64); its
-//     four epilogue warps rescale O when asked and write the normalised output.
+//     eight epilogue warps rescale O when asked and write the normalised output.
 // The split keeps both 256 KB accumulators on chip without recomputing S: O alone
 // fills a whole SM's tensor memory, and the query alone would fill most of its
 // shared memory.  P travels through L2 rather than distributed shared memory,
@@ -46,14 +50,13 @@ constexpr int kBoxesS = kD / 64;     // 9 blocks per page for scoring (c and k^R
 constexpr int kBoxesV = kDc / 64;    // 8 blocks per page for the value side (c only)
 constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page
 constexpr uint32_t kStageV = kBoxesV / 2 * kBoxBytes;  // 32768: half of a page's latent columns
-constexpr int kStagesS = 3;          // score CTA page stages
+constexpr int kStagesS = 2;          // score CTA page stages
 constexpr int kStagesV = 5;          // accumulate CTA half-page stages (two per page)
 constexpr int kPBufs = 3;            // accumulate CTA: P messages held in shared memory
 constexpr int kRing = 16;            // P messages in flight through global memory, per CTA pair
 constexpr int kBatch = 4;            // messages published together (one cluster-scope release each)
 constexpr int kShippers = 1;         // threads publishing batches, round robin
 constexpr int kRingBatches = kRing / kBatch;
-constexpr int kPrefetch = 8;         // pages prefetched into L2 ahead of the page being loaded
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
 constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one ring slot in global memory
@@ -61,10 +64,9 @@ constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (fact
 constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns
-constexpr int kIssuers = 3;          // score CTA MMA issuers, one partial S tile each
-constexpr int kBlocksPerIssuer = kBoxesS / kIssuers;  // 3 column blocks = 12 MMAs each
-constexpr uint32_t kTmemS = 0;       // score CTA: the page's three partial S tiles at 0, 64, 128
-constexpr uint32_t kTmemQ = 64 * kIssuers;  // score CTA: Q (bf16 pairs) at 192 .. 479
+constexpr int kIssuers = 2;          // score CTA MMA issuers: column blocks 0-3 | 4-7 and the RoPE block 8
+constexpr uint32_t kTmemS = 0;       // score CTA: partial S tiles [buffer b][issuer j] at 128 b + 64 j
+constexpr uint32_t kTmemQ = 256;     // score CTA: Q content part (blocks 0-7, bf16 pairs) at 256 .. 511
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory (offsets from a 1024-aligned base).  Score CTA: page stages at 0.
@@ -74,14 +76,15 @@ constexpr uint32_t kOffPBuf = kStagesV * kStageV;                   // accumulat
 constexpr uint32_t kOffMeta = kOffPBuf + kPBufs * kPBytes;          // accumulate: kPBufs x 1 KB
 constexpr uint32_t kOffEvt = kOffMeta + kPBufs * kMetaBytes;        // accumulate: alpha / inv_l, type
 constexpr uint32_t kAccumEnd = kOffEvt + 1040;
-constexpr uint32_t kScoreEnd = kStagesS * kStageS;
+constexpr uint32_t kOffQR = kStagesS * kStageS;   // score: Q RoPE block, UMMA K-major SW128, 16 KB
+constexpr uint32_t kScoreEnd = kOffQR + kHeads * 128;
 constexpr uint32_t kOffBar = kScoreEnd > kAccumEnd ? kScoreEnd : kAccumEnd;
 constexpr int kStagesMax = kStagesS > kStagesV ? kStagesS : kStagesV;
 constexpr int kBarFull = 0;                          // page stages (score) / half-page stages (accumulate)
 constexpr int kBarEmpty = kBarFull + kStagesMax;
-constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: partial S tile written (one per issuer)
-constexpr int kBarSEmpty = kBarSFull + kIssuers;     // score: all partial tiles read by the softmax warps
-constexpr int kBarQReady = kBarSEmpty + 1;           // score: the item's Q is in TMEM
+constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: partial S tile written, [issuer][buffer]
+constexpr int kBarSEmpty = kBarSFull + 2 * kIssuers; // score: a buffer's partial tiles read by the softmax warps
+constexpr int kBarQReady = kBarSEmpty + 2;           // score: the item's Q is in TMEM and shared memory
 constexpr int kBarPFree = kBarQReady + 1;            // score: ring slot consumed (partner arrives)
 constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a batch of ring slots written (partner arrives)
 constexpr int kBarPStaged = kBarPReady + kRingBatches;  // score: all rows of a ring slot written
@@ -102,7 +105,8 @@ constexpr uint32_t kDecodeSmem = kOffXSum + 2 * 2 * kHeads * 4 + 1024;  // + sla
 constexpr int kDecodeThreads = (12 + kShippers) * 32;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpShipper = 12;
 static_assert(kDecodeSmem <= 227u * 1024u, "decode kernel shared memory exceeds the per-CTA limit");
-static_assert(kTmemQ + 32u * kBoxesS <= kTmemCols, "score CTA tensor memory overflow");
+static_assert(kTmemQ + 32u * (kBoxesS - 1) <= kTmemCols && kTmemS + 128u * 2 <= kTmemQ,
+              "score CTA tensor memory overflow");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);    // A = Q (TMEM), B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A = P K-major, B = V MN-major
@@ -138,7 +142,6 @@ struct DecodeParams {
     float *part_o;                // [slots, 128, 512]
     float *part_lse;              // [slots, 128]
     uint8_t *ring;                // [clusters, kRing, kMsgBytes] P messages
-    const uint8_t *pool;          // [num_pages, 64, 576] bf16 (for L2 prefetches)
     int B, Tq, causal, num_pages, max_pages;
     float sl2;                    // scale * log2(e)
 };
@@ -365,12 +368,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
         : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z, uint64_t pol) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y), "r"(z), "l"(pol)
-                 : "memory");
-}
 // global -> shared::cta bulk copy, completion counted on a local barrier
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
                                               uint64_t pol) {
@@ -379,13 +376,6 @@ __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uin
             dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
-}
-// One warp asks L2 for a whole page (576 lines of 128 bytes), to be kept until its second
-// read; plain per-lane prefetches leave the TMA unit to the loads themselves.
-__device__ __forceinline__ void prefetch_page_l2(const uint8_t *page, int lane) {
-#pragma unroll
-    for (int k = 0; k < kStageS / 128 / 32; ++k)
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(page + (size_t)(k * 32 + lane) * 128) : "memory");
 }
 __device__ __forceinline__ void st_global_v4_hint(void *dst, uint4 v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x), "r"(v.y),
@@ -428,17 +418,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // Page producer (a whole warp; lane 0 issues).  The tensor map views the pool as (64 columns,
 // rows, column blocks) with strides (2 B, 1152 B, 128 B), so one box lands in shared memory as
 // `blocks` consecutive 64-row x 128-byte swizzled blocks -- the operand layout of the MMAs.
-// Block-table entries are read 32 tiles at a time (one per lane) and one chunk ahead.  With
-// `prefetch`, each load also asks L2 for the page kPrefetch tiles further on.
+// Block-table entries are read 32 tiles at a time (one per lane) and one chunk ahead.
+// `first_read`: this CTA reads each page first (L2 keeps it for the partner), else last.
 // kHalves = 2: each page is loaded as two half-page boxes (latent blocks 0-3 and 4-7) into
 // consecutive stages, so the value MMAs of one half can start and release independently.
 template <int kStages, int kHalves>
 __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                              uint32_t stage_bytes, bool prefetch, int cid, int ncl, int n_items,
+                                              uint32_t stage_bytes, bool first_read, int cid, int ncl, int n_items,
                                               volatile int *abort) {
     const int lane = threadIdx.x & 31;
     // the score CTA's read is a page's first: keep it for the partner; the partner's is its last
-    const uint64_t pol = prefetch ? l2_policy_evict_last() : l2_policy_evict_first();
+    const uint64_t pol = first_read ? l2_policy_evict_last() : l2_policy_evict_first();
     uint32_t g = 0;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
@@ -447,20 +437,13 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
         int cur = it.tb + lane < it.te ? checked_page(p, it.b, it.tb + lane) : 0;
         int nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
         int chunk = it.tb;
-        if (prefetch) {  // the item's first pages
-            for (int k = 0; k < kPrefetch && it.tb + k < it.te; ++k)
-                prefetch_page_l2(p.pool + (size_t)__shfl_sync(0xffffffffu, cur, k) * kStageS, lane);
-        }
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             if (tile - chunk == 32) {
                 chunk += 32;
                 cur = nxt;
                 nxt = chunk + 32 + lane < it.te ? checked_page(p, it.b, chunk + 32 + lane) : 0;
             }
-            const int idx = tile - chunk;
-            const int pg = __shfl_sync(0xffffffffu, cur, idx);
-            const int fidx = idx + kPrefetch;
-            const int fpg = __shfl_sync(0xffffffffu, fidx < 32 ? cur : nxt, fidx & 31);
+            const int pg = __shfl_sync(0xffffffffu, cur, tile - chunk);
 #pragma unroll
             for (int hf = 0; hf < kHalves; ++hf) {
                 const uint32_t u = g * kHalves + hf, s = u % kStages;
@@ -472,7 +455,6 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
                 }
                 __syncwarp();
             }
-            if (prefetch && tile + kPrefetch < it.te) prefetch_page_l2(p.pool + (size_t)fpg * kStageS, lane);
         }
     }
     g *= kHalves;
@@ -482,16 +464,14 @@ __device__ __forceinline__ void role_producer(const DecodeParams &p, const CUten
             if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
 }
 
-// Score CTA, MMA issuer `me` (0..2, one thread each).  All issuers work on every page: issuer
-// `me` accumulates column blocks 3me .. 3me+2 of S = Q . K_tile^T into partial tile `me`, in
-// fully unrolled steps with constant descriptor offsets.  One thread issues N = 64 MMAs too
-// slowly to keep the tensor pipe busy; three splitting each page do, and a page then leaves
-// its stage as soon as the tensor pipe is done with it.  The stage is free once all three
-// have committed.
+// Score CTA, MMA issuer `me` (0 or 1, one thread each).  Both issuers work on every page:
+// issuer 0 accumulates column blocks 0-3 of S = Q . K_tile^T into its partial tile, issuer 1
+// blocks 4-7 (A from TMEM) and the RoPE block 8 (A from shared memory), in fully unrolled
+// steps with constant descriptor offsets.  Page g uses partial-tile buffer g & 1, so the
+// issuers run up to a page ahead of the softmax warps.  A stage is free once both commit.
 __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, uint32_t me,
                                                int cid, int ncl, int n_items, volatile int *abort) {
     uint32_t g = 0, ic = 0;
-    const uint32_t bx0 = me * kBlocksPerIssuer;
     for (int r = 0;; ++r) {
         const int i = schedule(r, cid, ncl);
         if (i >= n_items) break;
@@ -501,20 +481,28 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
         tc_fence_after();
         ++ic;
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            const uint32_t s = g % kStagesS;
+            const uint32_t s = g % kStagesS, buf = g & 1u;
             if (!mbar_wait(sm.bar(kBarFull + s), (g / kStagesS) & 1u, abort)) return;
-            if (!mbar_wait(sm.bar(kBarSEmpty), (g & 1u) ^ 1u, abort)) return;
+            if (!mbar_wait(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort)) return;
             tc_fence_after();
-            const uint32_t d = tmem + kTmemS + me * 64u;
-            const uint32_t a0 = tmem + kTmemQ + bx0 * 32u;
-            const uint64_t b0 = sdesc_sw128(sm.stage(s, kStageS) + bx0 * kBoxBytes, 16u, 1024u);
+            const uint32_t d = tmem + kTmemS + buf * 128u + me * 64u;
+            const uint32_t a0 = tmem + kTmemQ + me * 4u * 32u;
+            const uint32_t st = sm.stage(s, kStageS);
+            const uint64_t b0 = sdesc_sw128(st + me * 4u * kBoxBytes, 16u, 1024u);
 #pragma unroll
-            for (int k = 0; k < 4 * kBlocksPerIssuer; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
                 mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS, k != 0);
             }
+            if (me == 1) {  // the RoPE block: both operands in shared memory
+                const uint64_t aq = sdesc_sw128(sm.base + kOffQR, 16u, 1024u);
+                const uint64_t br = sdesc_sw128(st + 8u * kBoxBytes, 16u, 1024u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(d, aq + (uint64_t)((32u * kk) >> 4), br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
+            }
             mma_commit(sm.bar(kBarEmpty + s));
-            mma_commit(sm.bar(kBarSFull + me));
+            mma_commit(sm.bar(kBarSFull + 2 * (int)me + (int)buf));
         }
     }
 }
@@ -545,12 +533,12 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             if (hf == 0) p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
             continue;
         }
-        // absorbed query of this head -> TMEM lane h (bf16 pairs, 288 columns; blocks 0-4 by the
-        // first half, 5-8 by the second).  The next block's loads are in flight while one block
-        // is stored, so the item start pays about one memory latency per two blocks.
+        // absorbed query of this head: the content part -> TMEM lane h (bf16 pairs, blocks 0-3 by
+        // the first half, 4-7 by the second), the RoPE part (block 8, second half) -> row h of the
+        // shared-memory operand.  The next block's loads are in flight while one block is stored.
         {
             const uint4 *q = reinterpret_cast<const uint4 *>(p.q_abs + ((size_t)it.bt * kHeads + h) * kD);
-            const int c0 = hf ? 5 : 0, c1 = hf ? kBoxesS : 5;
+            const int c0 = hf ? 4 : 0, c1 = hf ? 8 : 4;
             uint4 va[8], vb[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) va[u] = __ldg(q + c0 * 8 + u);
@@ -568,6 +556,17 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 }
                 if (has_b) tmem_st32(tmem + lane_off + kTmemQ + (c + 1) * 32u, *reinterpret_cast<const uint32_t(*)[32]>(vb));
             }
+            if (hf) {
+                const uint32_t qr = sm.base + kOffQR + row_off;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 x = __ldg(q + 8 * 8 + u);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qr + (uint32_t)((u ^ (h & 7)) * 16)),
+                                 "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();  // generic writes -> the MMAs (async proxy)
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarQReady));
@@ -577,22 +576,21 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
         // denominator then carry the same rounding, which matters when a few tokens dominate
         float m = 0.f, l = 0.f, lr = 0.f, lt = 0.f, lrt = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
+            const uint32_t buf = sc & 1u;
 #pragma unroll
-            for (int t = 0; t < kIssuers; ++t) MLA_WAIT_WARP(sm.bar(kBarSFull + t), sc & 1u, abort);
+            for (int t = 0; t < kIssuers; ++t) MLA_WAIT_WARP(sm.bar(kBarSFull + 2 * t + (int)buf), (sc >> 1) & 1u, abort);
             tc_fence_after();
             float s[32];
             {
-                uint32_t a[32], b[32], c3[32];
-                tmem_ld32(tmem + lane_off + kTmemS + 32u * hf, a);
-                tmem_ld32(tmem + lane_off + kTmemS + 64u + 32u * hf, b);
-                tmem_ld32(tmem + lane_off + kTmemS + 128u + 32u * hf, c3);
+                uint32_t a[32], b[32];
+                tmem_ld32(tmem + lane_off + kTmemS + buf * 128u + 32u * hf, a);
+                tmem_ld32(tmem + lane_off + kTmemS + buf * 128u + 64u + 32u * hf, b);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    s[c] = (__uint_as_float(a[c]) + __uint_as_float(b[c])) + __uint_as_float(c3[c]);
+                for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(a[c]) + __uint_as_float(b[c]);
             }
             tc_fence_before();
-            mbar_arrive(sm.bar(kBarSEmpty));
+            mbar_arrive(sm.bar(kBarSEmpty + (int)buf));
 
             const int valid = min(kPage, it.n_vis - tile * kPage) - 32 * hf;  // columns of this half
             if (valid < 32) {
@@ -963,8 +961,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
             mbar_init(sm.bar(kBarFull + s), 1);
             mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? kIssuers : 1);  // score: every issuer commits
         }
-        for (int j = 0; j < kIssuers; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
-        mbar_init(sm.bar(kBarSEmpty), 256);  // every softmax thread
+        for (int j = 0; j < 2 * kIssuers; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
+        for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSEmpty + j), 256);  // every softmax thread
         mbar_init(sm.bar(kBarQReady), 256);
         for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPFree + j), 1);  // score CTA: the partner's releaser
         for (int j = 0; j < kRingBatches; ++j) mbar_init(sm.bar(kBarPReady + j), 1);  // accumulate CTA: the shipper
@@ -1006,9 +1004,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
             role_producer<kStagesS, 1>(p, &tmap_s, sm, kStageS, true, cid, ncl, n_items, abort);
         else
             role_producer<kStagesV, 2>(p, &tmap_v, sm, kStageV, false, cid, ncl, n_items, abort);
-    } else if (warp < kWarpMma + kIssuers) {
+    } else if (warp < kWarpMma + 3) {
         if (rank == 0) {
-            if (lane0) role_score_mma(p, sm, tmem, (uint32_t)(warp - kWarpMma), cid, ncl, n_items, abort);
+            if (warp < kWarpMma + kIssuers && lane0)
+                role_score_mma(p, sm, tmem, (uint32_t)(warp - kWarpMma), cid, ncl, n_items, abort);
         } else if (warp == kWarpMma) {
             role_accum_mma(p, sm, tmem, cid, ncl, n_items, abort);
         } else if (warp == kWarpMma + 1) {

@@ -51,6 +51,13 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
         d.supported = (prop.major == 10 && prop.minor == 3);
         d.sms = prop.multiProcessorCount;
         if (d.supported) {
+            // every kernel of a decode call asks for the maximum shared-memory carveout, so the
+            // SMs need not switch their L1 / shared split between the plan, decode and combine
+            for (const void *fn : {(const void *)plan_kernel, (const void *)combine_kernel,
+                                   (const void *)combine_rows_kernel, (const void *)decode_kernel})
+                cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+            cudaGetLastError();
             if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmem) !=
                     cudaSuccess ||
                 cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
@@ -348,7 +355,6 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
     p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
     p.ring = ws + w.ring;
-    p.pool = static_cast<const uint8_t *>(kv_pool);
     p.B = batch;
     p.Tq = q_len;
     p.causal = causal ? 1 : 0;
