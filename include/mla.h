@@ -132,7 +132,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
  *
  * Limit: requests whose mla_decode_workspace_size(batch, q_len, num_splits) exceeds
  * MLA_STATIC_SCRATCH_BYTES are rejected with MLA_ERR_WORKSPACE before anything is
- * enqueued.  With the automatic plan (num_splits = 0) that admits batch * q_len up to 143.
+ * enqueued.  With the automatic plan (num_splits = 0) that admits batch * q_len up to 90.
  *
  * First call per device: it looks up the device address of the array (with that
  * device current), once; make that first call before any stream capture begins.

@@ -48,76 +48,79 @@ constexpr int kPage = 64;            // tokens per page == tokens per tile
 constexpr int kBoxBytes = kPage * 128;  // one 64-row x 64-column bf16 block (128-byte rows)
 constexpr int kBoxesS = kD / 64;     // 9 blocks per page for scoring (c and k^R)
 constexpr int kBoxesV = kDc / 64;    // 8 blocks per page for the value side (c only)
-constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page
-constexpr uint32_t kStageV = kBoxesV / 2 * kBoxBytes;  // 32768: half of a page's latent columns
-constexpr int kStagesS = 2;          // score CTA page stages
-constexpr int kStagesV = 5;          // accumulate CTA half-page stages (two per page)
-constexpr int kPBufs = 3;            // accumulate CTA: P messages held in shared memory
+constexpr uint32_t kStageS = kBoxesS * kBoxBytes;  // 73728: one whole page (score CTA stage)
+constexpr int kStagesS = 3;          // score CTA page stages
+constexpr uint32_t kQRopeOff = 4 * kHeads * 128;  // in a query stage: 4 content blocks, then 64 heads' RoPE block
+constexpr uint32_t kStageV = kBoxesV * kBoxBytes;  // 65536: a page's 512 latent columns (accumulate CTA stage)
+constexpr int kStagesV = 2;          // accumulate CTA page stages
+constexpr int kPBufs = 4;            // accumulate CTA: P messages held in shared memory
 constexpr int kRing = 16;            // P messages in flight through global memory, per CTA pair
-constexpr int kBatch = 4;            // messages published together (one cluster-scope release each)
-constexpr int kShippers = 1;         // threads publishing batches, round robin
-constexpr int kRingBatches = kRing / kBatch;
+constexpr int kMaxBatch = 4;         // messages published together (one cluster-scope release each)
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
-constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one ring slot in global memory
+constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one message: P, then its factors
 constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (factor 256)
 constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns
 constexpr int kIssuers = 2;          // score CTA MMA issuers: column blocks 0-3 | 4-7 and the RoPE block 8
-constexpr uint32_t kTmemS = 0;       // score CTA: partial S tiles [buffer b][issuer j] at 128 b + 64 j
+constexpr uint32_t kTmemS = 0;       // score CTA: S tile of buffer b at 64 b
+constexpr uint32_t kTmemQR = 128;    // score CTA: Q RoPE part (block 8, bf16 pairs) at 128 .. 159
 constexpr uint32_t kTmemQ = 256;     // score CTA: Q content part (blocks 0-7, bf16 pairs) at 256 .. 511
 constexpr uint32_t kTmemCols = 512;
 
-// Shared memory (offsets from a 1024-aligned base).  Score CTA: page stages at 0.
-// Accumulate CTA: half-page stages at 0, P buffers, their factors, the event buffer.
+// Shared memory (offsets from a 1024-aligned base).  Score CTA: three page stages at 0 (an
+// item's query passes through the first two of its positions).  Accumulate CTA: two page
+// stages at 0, the P buffers (each a whole message: P, then its factors), the event buffer.
 // Barriers sit at the same offset in both CTAs (the partner arrives on them).
-constexpr uint32_t kOffPBuf = kStagesV * kStageV;                   // accumulate: kPBufs x 16 KB
-constexpr uint32_t kOffMeta = kOffPBuf + kPBufs * kPBytes;          // accumulate: kPBufs x 1 KB
-constexpr uint32_t kOffEvt = kOffMeta + kPBufs * kMetaBytes;        // accumulate: alpha / inv_l, type
+constexpr uint32_t kOffPBuf = kStagesV * kStageV;                   // accumulate: kPBufs x 17 KB
+constexpr uint32_t kOffEvt = kOffPBuf + kPBufs * kMsgBytes;         // accumulate: alpha / inv_l, type, P buffer
 constexpr uint32_t kAccumEnd = kOffEvt + 1040;
-constexpr uint32_t kOffQR = kStagesS * kStageS;   // score: Q RoPE block, UMMA K-major SW128, 16 KB
-constexpr uint32_t kScoreEnd = kOffQR + kHeads * 128;
+constexpr uint32_t kScoreEnd = kStagesS * kStageS;
 constexpr uint32_t kOffBar = kScoreEnd > kAccumEnd ? kScoreEnd : kAccumEnd;
 constexpr int kStagesMax = kStagesS > kStagesV ? kStagesS : kStagesV;
-constexpr int kBarFull = 0;                          // page stages (score) / half-page stages (accumulate)
+constexpr int kBarFull = 0;                          // page stages
 constexpr int kBarEmpty = kBarFull + kStagesMax;
-constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: partial S tile written, [issuer][buffer]
-constexpr int kBarSEmpty = kBarSFull + 2 * kIssuers; // score: a buffer's partial tiles read by the softmax warps
+constexpr int kBarSHalf = kBarEmpty + kStagesMax;    // score: issuer 0's part of S tile [buffer] done
+constexpr int kBarSFull = kBarSHalf + 2;             // score: S tile [buffer] complete
+constexpr int kBarSEmpty = kBarSFull + 2;            // score: S tile [buffer] read by the softmax warps
 constexpr int kBarQReady = kBarSEmpty + 2;           // score: the item's Q is in TMEM and shared memory
 constexpr int kBarPFree = kBarQReady + 1;            // score: ring slot consumed (partner arrives)
-constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a batch of ring slots written (partner arrives)
-constexpr int kBarPStaged = kBarPReady + kRingBatches;  // score: all rows of a ring slot written
+constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a ring slot written (partner arrives)
+constexpr int kBarPStaged = kBarPReady + kRing;      // score: all rows of a ring slot written
 constexpr int kBarPFull = kBarPStaged + kRing;       // accumulate: P buffer landed
 constexpr int kBarPBufFree = kBarPFull + kPBufs;     // accumulate: P buffer used by the MMAs and the releaser
 constexpr int kBarMmaEvt = kBarPBufFree + kPBufs;    // accumulate: event for the epilogue warps
 constexpr int kBarCorrEvt = kBarMmaEvt + 1;          // accumulate: event served
-constexpr int kBarXMax = kBarCorrEvt + 1;            // score: row-max swap, [quadrant][page parity]
-constexpr int kBarXSum = kBarXMax + 8;               // score: row-sum swap, [quadrant]
+constexpr int kBarXSum = kBarCorrEvt + 1;            // score: row-sum swap, [quadrant]
 constexpr int kNumBars = kBarXSum + 4;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kOffXMax = (kOffAbort + 4 + 15u) & ~15u;   // score: row-max exchange [2][2][128] f32
-constexpr uint32_t kOffXSum = kOffXMax + 2 * 2 * kHeads * 4;  // score: row-sum exchange [2 sums][2][128] f32
+constexpr uint32_t kOffXSum = (kOffAbort + 4 + 15u) & ~15u;  // score: row-sum exchange [2 sums][2][128] f32
 constexpr uint32_t kDecodeSmem = kOffXSum + 2 * 2 * kHeads * 4 + 1024;  // + slack to align the base
-// warps: 0-7 softmax (score) / epilogue (accumulate), 8 page producer, 9-11 the three score
-// MMA issuers (score) / PV MMA, P loader, releaser (accumulate), 12 shipper (score)
-constexpr int kDecodeThreads = (12 + kShippers) * 32;
+// warps: 0-7 softmax (score) / epilogue (accumulate), 8 page producer, 9-10 the two score MMA
+// issuers (score) / 9-11 PV MMA, P loader, releaser (accumulate), 12 shipper (score)
+constexpr int kDecodeThreads = 13 * 32;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpShipper = 12;
 static_assert(kDecodeSmem <= 227u * 1024u, "decode kernel shared memory exceeds the per-CTA limit");
-static_assert(kTmemQ + 32u * (kBoxesS - 1) <= kTmemCols && kTmemS + 128u * 2 <= kTmemQ,
+static_assert(kTmemQ + 32u * (kBoxesS - 1) <= kTmemCols && kTmemS + 64u * 2 <= kTmemQR && kTmemQR + 32u <= kTmemQ,
               "score CTA tensor memory overflow");
+static_assert(kMsgBytes % 1024 == 0, "P buffers must stay 1024-byte aligned (128-byte swizzle atoms)");
+static_assert(2 * kStageS == 8 * kHeads * 128 + kHeads * 128, "an item's query fills the two score stages");
+// the epilogue stages its output through the P buffer of the item's last page: 2 KB per warp
+static_assert(8 * 2048 <= kPBytes, "epilogue staging does not fit a P buffer");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);    // A = Q (TMEM), B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A = P K-major, B = V MN-major
 
 constexpr uint32_t kEvtRescale = 1u, kEvtEpilogue = 2u;
 
-// One unit of work: tiles [tb, te) of query (b, t) where bt = b * Tq + t.
-// slot < 0: the item covers the whole query and writes the final output;
-// slot >= 0: it writes a partial (o / l in fp32, lse) into workspace slot `slot`.
-struct Item {
-    int bt, tb, te, slot;
+// One unit of work: tiles [tb, te) of query (b, t) where bt = b * Tq + t, whose visible
+// prefix is n_vis tokens.  slot < 0: the item covers the whole query and writes the final
+// output; slot >= 0: it writes a partial (o / l in fp32, lse) into workspace slot `slot`.
+// 32 bytes, read as two 16-byte loads.
+struct __align__(16) Item {
+    int bt, tb, te, slot, b, n_vis, pad0, pad1;
 };
 struct PlanHeader {
     int n_items;
@@ -138,11 +141,11 @@ struct DecodeParams {
     __nv_bfloat16 *o_lat;         // [B, Tq, 128, 512]
     float *lse;                   // [B, Tq, 128]
     const PlanHeader *hdr;
-    const Item *items;
+    const Item *items;            // max_items entries
     float *part_o;                // [slots, 128, 512]
     float *part_lse;              // [slots, 128]
     uint8_t *ring;                // [clusters, kRing, kMsgBytes] P messages
-    int B, Tq, causal, num_pages, max_pages;
+    int B, Tq, causal, num_pages, max_pages, max_items;
     float sl2;                    // scale * log2(e)
 };
 
@@ -157,17 +160,15 @@ __device__ __forceinline__ int visible_tokens(int L, int Tq, int t, int causal) 
 }
 
 __device__ __forceinline__ ItemInfo load_item(const DecodeParams &p, int i) {
-    Item it = p.items[i];
+    const int4 *src = reinterpret_cast<const int4 *>(p.items + i);
+    const int4 a = src[0], c = src[1];
     ItemInfo x;
-    x.bt = it.bt;
-    x.b = it.bt / p.Tq;
-    int t = it.bt - x.b * p.Tq;
-    x.tb = it.tb;
-    x.te = it.te;
-    x.slot = it.slot;
-    int L = p.seq_lens[x.b];
-    L = L < 0 ? 0 : (L > p.max_pages * kPage ? p.max_pages * kPage : L);
-    x.n_vis = visible_tokens(L, p.Tq, t, p.causal);
+    x.bt = a.x;
+    x.tb = a.y;
+    x.te = a.z;
+    x.slot = a.w;
+    x.b = c.x;
+    x.n_vis = c.y;
     return x;
 }
 
@@ -176,6 +177,19 @@ __device__ __forceinline__ ItemInfo load_item(const DecodeParams &p, int i) {
 __device__ __forceinline__ int schedule(int r, int cid, int ncl) {
     return r * ncl + ((r & 1) ? (ncl - 1 - cid) : cid);
 }
+
+// A cluster's walk over its items.  The first item (round 0 is item `cid`) is read together
+// with the plan header, before the item count is known, so the two reads overlap.
+struct Sched {
+    int cid, ncl, n_items;
+    ItemInfo first;
+    __device__ __forceinline__ bool get(const DecodeParams &p, int r, ItemInfo &it) const {
+        const int i = schedule(r, cid, ncl);
+        if (i >= n_items) return false;
+        it = r == 0 ? first : load_item(p, i);
+        return true;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // Plan: split counts, items (longest first), partial slots.  One CTA.
@@ -317,9 +331,16 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
         in.tiles = tiles[bt];
         in.item_off = item_off[bt];
         info[bt] = in;
+        const int b = bt / Tq;
+        int L = seq_lens[b];
+        L = L < 0 ? 0 : (L > max_pages * kPage ? max_pages * kPage : L);
+        const int n_vis = visible_tokens(L, Tq, bt - b * Tq, causal);
         for (int j = 0; j < in.splits; ++j) {
             Item it;
             it.bt = bt;
+            it.b = b;
+            it.n_vis = n_vis;
+            it.pad0 = it.pad1 = 0;
             it.tb = (int)(((long long)in.tiles * j) / in.splits);
             it.te = (int)(((long long)in.tiles * (j + 1)) / in.splits);
             it.slot = in.splits > 1 ? in.slot_base + j : -1;
@@ -342,8 +363,8 @@ struct Smem {
     uint32_t base;  // shared::cta address of the aligned base
     __device__ __forceinline__ uint32_t bar(int i) const { return base + kOffBar + 8u * i; }
     __device__ __forceinline__ uint32_t stage(uint32_t s, uint32_t bytes) const { return base + s * bytes; }
-    __device__ __forceinline__ uint32_t pbuf(uint32_t j) const { return base + kOffPBuf + j * kPBytes; }
-    __device__ __forceinline__ uint32_t meta(uint32_t j) const { return base + kOffMeta + j * kMetaBytes; }
+    __device__ __forceinline__ uint32_t pbuf(uint32_t j) const { return base + kOffPBuf + j * kMsgBytes; }
+    __device__ __forceinline__ uint32_t meta(uint32_t j) const { return pbuf(j) + kPBytes; }
     __device__ __forceinline__ uint32_t evt() const { return base + kOffEvt; }
 };
 
@@ -382,6 +403,12 @@ __device__ __forceinline__ void st_global_v4_hint(void *dst, uint4 v, uint64_t p
                  "r"(v.z), "r"(v.w), "l"(pol)
                  : "memory");
 }
+__device__ __forceinline__ void st_global_v8_hint(void *dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                                  uint32_t f, uint32_t g, uint32_t h, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void st_global_f32_hint(void *dst, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(pol) : "memory");
 }
@@ -415,161 +442,215 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 #define MLA_WAIT_WARP(bar_, par_, ab_) \
     if (__any_sync(0xffffffffu, !mbar_wait(bar_, par_, ab_))) return
 
-// Page producer (a whole warp; lane 0 issues).  The tensor map views the pool as (64 columns,
-// rows, column blocks) with strides (2 B, 1152 B, 128 B), so one box lands in shared memory as
-// `blocks` consecutive 64-row x 128-byte swizzled blocks -- the operand layout of the MMAs.
-// Block-table entries are read 32 tiles at a time (one per lane) and one chunk ahead.
-// `first_read`: this CTA reads each page first (L2 keeps it for the partner), else last.
-// kHalves = 2: each page is loaded as two half-page boxes (latent blocks 0-3 and 4-7) into
-// consecutive stages, so the value MMAs of one half can start and release independently.
-template <int kStages, int kHalves>
-__device__ __forceinline__ void role_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                              uint32_t stage_bytes, bool first_read, int cid, int ncl, int n_items,
-                                              volatile int *abort) {
+// Page ids of an item, read from the block table 32 tiles at a time (one per lane), one chunk
+// ahead of use.
+struct PageIds {
+    int cur, nxt, chunk;
+    __device__ __forceinline__ void start(const DecodeParams &p, const ItemInfo &it, int lane) {
+        chunk = it.tb;
+        cur = it.tb + lane < it.te ? checked_page(p, it.b, it.tb + lane) : 0;
+        nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
+    }
+    // page of `tile` (tiles visited in order); warp-collective
+    __device__ __forceinline__ int get(const DecodeParams &p, const ItemInfo &it, int tile, int lane) {
+        if (tile - chunk == 32) {
+            chunk += 32;
+            cur = nxt;
+            nxt = chunk + 32 + lane < it.te ? checked_page(p, it.b, chunk + 32 + lane) : 0;
+        }
+        return __shfl_sync(0xffffffffu, cur, tile - chunk);
+    }
+};
+
+// Accumulate CTA, page producer (a whole warp; lane 0 issues): one box per page, its 512 latent
+// columns (blocks 0-7), into a 2-stage ring.  One large box rather than several small ones:
+// the TMA engine has a fixed cost per box of the order of the transfer of 40 KB.  The tensor
+// map views the pool as (64 columns, rows, 9 column blocks) with strides (2 B, 1152 B, 128 B),
+// so a box lands as consecutive 64-row x 128-byte swizzled blocks -- the MMAs' operand layout.
+// These reads are a page's second: L2 may drop the lines afterwards (evict_first).
+__device__ __forceinline__ void role_value_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
+                                                    const Sched &sc, volatile int *abort) {
     const int lane = threadIdx.x & 31;
-    // the score CTA's read is a page's first: keep it for the partner; the partner's is its last
-    const uint64_t pol = first_read ? l2_policy_evict_last() : l2_policy_evict_first();
-    uint32_t g = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
-        int cur = it.tb + lane < it.te ? checked_page(p, it.b, it.tb + lane) : 0;
-        int nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
-        int chunk = it.tb;
-        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            if (tile - chunk == 32) {
-                chunk += 32;
-                cur = nxt;
-                nxt = chunk + 32 + lane < it.te ? checked_page(p, it.b, chunk + 32 + lane) : 0;
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t u = 0;
+    ItemInfo it;
+    PageIds ids;
+    for (int r = 0; sc.get(p, r, it); ++r) {
+        ids.start(p, it, lane);
+        for (int tile = it.tb; tile < it.te; ++tile, ++u) {
+            const int pg = ids.get(p, it, tile, lane);
+            const uint32_t s = u % kStagesV;
+            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesV) & 1u) ^ 1u, abort)) return;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageV);
+                tma_load_3d(sm.stage(s, kStageV), tmap, 0, pg * kPage, 0, sm.bar(kBarFull + s), pol);
             }
-            const int pg = __shfl_sync(0xffffffffu, cur, tile - chunk);
-#pragma unroll
-            for (int hf = 0; hf < kHalves; ++hf) {
-                const uint32_t u = g * kHalves + hf, s = u % kStages;
-                if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStages) & 1u) ^ 1u, abort)) return;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(sm.bar(kBarFull + s), stage_bytes);
-                    tma_load_3d(sm.stage(s, stage_bytes), tmap, 0, pg * kPage, hf * (kBoxesV / 2),
-                                sm.bar(kBarFull + s), pol);
-                }
-                __syncwarp();
-            }
+            __syncwarp();
         }
     }
-    g *= kHalves;
     // let every load issued land before the CTA can retire (bounded)
     if (lane == 0)
-        for (uint32_t k = (g > kStages ? g - kStages : 0); k < g; ++k)
-            if (!mbar_wait(sm.bar(kBarFull + k % kStages), (k / kStages) & 1u, abort)) return;
+        for (uint32_t k = (u > kStagesV ? u - kStagesV : 0); k < u; ++k)
+            if (!mbar_wait(sm.bar(kBarFull + k % kStagesV), (k / kStagesV) & 1u, abort)) return;
 }
 
-// Score CTA, MMA issuer `me` (0 or 1, one thread each).  Both issuers work on every page:
-// issuer 0 accumulates column blocks 0-3 of S = Q . K_tile^T into its partial tile, issuer 1
-// blocks 4-7 (A from TMEM) and the RoPE block 8 (A from shared memory), in fully unrolled
-// steps with constant descriptor offsets.  Page g uses partial-tile buffer g & 1, so the
-// issuers run up to a page ahead of the softmax warps.  A stage is free once both commit.
-__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, uint32_t me,
-                                               int cid, int ncl, int n_items, volatile int *abort) {
-    uint32_t g = 0, ic = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+// Score CTA, page producer (a whole warp; lane 0 issues).  Its stage sequence holds, per item,
+// first the absorbed query -- position 0: column blocks 0-3 of all heads and the RoPE block of
+// heads 0-63; position 1: blocks 4-7 and the RoPE block of heads 64-127, which exactly fills the
+// two stages of its positions -- and then one whole page per position.  Every transfer is one
+// large box (the TMA engine's cost per box is high).  Pages are read first here: L2 keeps them for
+// the partner (evict_last); the query is read once (evict_first).
+__device__ __forceinline__ void role_score_producer(const DecodeParams &p, const CUtensorMap *pages,
+                                                    const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
+                                                    const Sched &sc, volatile int *abort) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+    uint32_t u = 0;
+    ItemInfo it;
+    PageIds ids;
+    for (int r = 0; sc.get(p, r, it); ++r) {
+        if (it.te <= it.tb) continue;
+        ids.start(p, it, lane);
+        const int row0 = it.bt * kHeads;
+        for (int hq = 0; hq < 2; ++hq, ++u) {
+            const uint32_t s = u % kStagesS;
+            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
+                tma_load_3d(sm.stage(s, kStageS), qc, 0, row0, 4 * hq, sm.bar(kBarFull + s), once);
+                tma_load_3d(sm.stage(s, kStageS) + kQRopeOff, qr, 0, row0 + 64 * hq, kBoxesS - 1, sm.bar(kBarFull + s),
+                            once);
+            }
+            __syncwarp();
+        }
+        for (int tile = it.tb; tile < it.te; ++tile, ++u) {
+            const int pg = ids.get(p, it, tile, lane);
+            const uint32_t s = u % kStagesS;
+            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
+                tma_load_3d(sm.stage(s, kStageS), pages, 0, pg * kPage, 0, sm.bar(kBarFull + s), keep);
+            }
+            __syncwarp();
+        }
+    }
+    // let every load issued land before the CTA can retire (bounded)
+    if (lane == 0)
+        for (uint32_t k = (u > kStagesS ? u - kStagesS : 0); k < u; ++k)
+            if (!mbar_wait(sm.bar(kBarFull + k % kStagesS), (k / kStagesS) & 1u, abort)) return;
+}
+
+// Score CTA, MMA issuer kMe (one thread each).  One thread cannot issue N = 64 MMAs fast enough
+// to keep the tensor pipe busy, two can: issuer 0 computes column blocks 0-3 of S = Q . K_tile^T
+// into the page's S tile, and issuer 1, once that part has completed, accumulates blocks 4-7 and
+// the RoPE block 8 onto it (A from TMEM throughout).  Page g uses S buffer g & 1, so issuer 0
+// works on page g + 1 while issuer 1 finishes page g.  A stage is free once both have committed.
+// The two query stages are handed back (one plain arrival each) once the softmax warps report
+// the query in TMEM.
+template <int kMe>
+__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+                                               volatile int *abort) {
+    uint32_t g = 0, ic = 0, u = 0;
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) continue;
         if (!mbar_wait(sm.bar(kBarQReady), ic & 1u, abort)) return;
         tc_fence_after();
         ++ic;
-        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            const uint32_t s = g % kStagesS, buf = g & 1u;
-            if (!mbar_wait(sm.bar(kBarFull + s), (g / kStagesS) & 1u, abort)) return;
-            if (!mbar_wait(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort)) return;
+        mbar_arrive(sm.bar(kBarEmpty + u % kStagesS));
+        mbar_arrive(sm.bar(kBarEmpty + (u + 1) % kStagesS));
+        u += 2;
+        for (int tile = it.tb; tile < it.te; ++tile, ++g, ++u) {
+            const uint32_t s = u % kStagesS, buf = g & 1u;
+            if (!mbar_wait(sm.bar(kBarFull + s), (u / kStagesS) & 1u, abort)) return;
+            if (kMe == 0) {
+                if (!mbar_wait(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort)) return;
+            } else {
+                if (!mbar_wait(sm.bar(kBarSHalf + (int)buf), (g >> 1) & 1u, abort)) return;
+            }
             tc_fence_after();
-            const uint32_t d = tmem + kTmemS + buf * 128u + me * 64u;
-            const uint32_t a0 = tmem + kTmemQ + me * 4u * 32u;
+            const uint32_t d = tmem + kTmemS + buf * 64u;
+            const uint32_t a0 = tmem + kTmemQ + kMe * 4u * 32u;
             const uint32_t st = sm.stage(s, kStageS);
-            const uint64_t b0 = sdesc_sw128(st + me * 4u * kBoxBytes, 16u, 1024u);
+            const uint64_t b0 = sdesc_sw128(st + kMe * 4u * kBoxBytes, 16u, 1024u);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
-                mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS, k != 0);
+                mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS,
+                       kMe == 1 || k != 0);
             }
-            if (me == 1) {  // the RoPE block: both operands in shared memory
-                const uint64_t aq = sdesc_sw128(sm.base + kOffQR, 16u, 1024u);
+            if (kMe == 1) {  // the RoPE block
                 const uint64_t br = sdesc_sw128(st + 8u * kBoxBytes, 16u, 1024u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(d, aq + (uint64_t)((32u * kk) >> 4), br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
+                    mma_ts(d, tmem + kTmemQR + kk * 8u, br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
             }
             mma_commit(sm.bar(kBarEmpty + s));
-            mma_commit(sm.bar(kBarSFull + 2 * (int)me + (int)buf));
+            mma_commit(sm.bar((kMe == 0 ? kBarSHalf : kBarSFull) + (int)buf));
         }
     }
 }
 
 // Score CTA, softmax warps.  Eight warps, two per sub-partition: warp w owns heads
 // 32(w%4) .. 32(w%4)+31 (its TMEM lane quadrant) and columns [32 hf, 32 hf + 32) of each page,
-// hf = w / 4.  The two threads of a head swap their row maxima through shared memory every
-// page (and their row sums on an item's last page), so both take identical rescale decisions.
-// Per page: add the partial S tiles, online softmax with lazy rescaling, write the half-row of
-// the P message (bf16 in the UMMA K-major 128-byte-swizzle image, the rescale factor, and 1/l on
-// the item's last page) into the ring, then signal the shipper.
-__device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
-                                             int ncl, int n_items, volatile int *abort) {
-    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2;
-    const int h = q4 * 32 + (threadIdx.x & 31);
+// hf = w / 4.  Both threads of a head read the whole S row to take its maximum, so they make
+// identical rescale decisions without exchanging anything; they swap their row sums through
+// shared memory on an item's last page.  Per page: online softmax with lazy rescaling, write the
+// half-row of the P message (bf16 in the UMMA K-major 128-byte-swizzle image, the rescale factor,
+// and 1/l on the item's last page) into the ring, then signal the shipper.
+__device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &scd,
+                                             volatile int *abort) {
+    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2, lane = threadIdx.x & 31;
+    const int h = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.sl2;
     const uint32_t row_off = (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u;
-    uint8_t *const ring = p.ring + (size_t)cid * kRing * kMsgBytes;
-    const uint32_t xmax = sm.base + kOffXMax, xsum = sm.base + kOffXSum;
+    uint8_t *const ring = p.ring + (size_t)scd.cid * kRing * kMsgBytes;
+    const uint32_t xsum = sm.base + kOffXSum;
     const uint64_t keep = l2_policy_evict_last();
-    uint32_t sc = 0, nsum = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+    uint32_t sc = 0, nsum = 0, us = 0;
+    ItemInfo it;
+    for (int r = 0; scd.get(p, r, it); ++r) {
         if (it.te <= it.tb) {
             if (hf == 0) p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
             continue;
         }
-        // absorbed query of this head: the content part -> TMEM lane h (bf16 pairs, blocks 0-3 by
-        // the first half, 4-7 by the second), the RoPE part (block 8, second half) -> row h of the
-        // shared-memory operand.  The next block's loads are in flight while one block is stored.
+        // this head's absorbed query, from the item's two query stages (the previous item's MMAs
+        // are done: its last S tile has been read): content blocks 4 hf .. 4 hf + 3 -> TMEM lane h
+        // (bf16 pairs), and for hf = 1 the RoPE block -> TMEM lane h too.  Both stages hold
+        // 128-byte swizzled rows whose swizzle phase is h & 7.  The issuers free the stages.
         {
-            const uint4 *q = reinterpret_cast<const uint4 *>(p.q_abs + ((size_t)it.bt * kHeads + h) * kD);
-            const int c0 = hf ? 4 : 0, c1 = hf ? 8 : 4;
-            uint4 va[8], vb[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) va[u] = __ldg(q + c0 * 8 + u);
+            const uint32_t pc = us + (uint32_t)hf;
+            MLA_WAIT_WARP(sm.bar(kBarFull + pc % kStagesS), (pc / kStagesS) & 1u, abort);
+            const uint32_t stc = sm.stage(pc % kStagesS, kStageS) + (uint32_t)h * 128u;
 #pragma unroll 1
-            for (int c = c0; c < c1; c += 2) {
-                const bool has_b = c + 1 < c1, has_a2 = c + 2 < c1;
-                if (has_b) {
+            for (int bq = 0; bq < 4; ++bq) {
+                uint32_t v[32];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) vb[u] = __ldg(q + (c + 1) * 8 + u);
-                }
-                tmem_st32(tmem + lane_off + kTmemQ + c * 32u, *reinterpret_cast<const uint32_t(*)[32]>(va));
-                if (has_a2) {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) va[u] = __ldg(q + (c + 2) * 8 + u);
-                }
-                if (has_b) tmem_st32(tmem + lane_off + kTmemQ + (c + 1) * 32u, *reinterpret_cast<const uint32_t(*)[32]>(vb));
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                                 : "r"(stc + (uint32_t)bq * (kHeads * 128u) + (uint32_t)((c ^ (lane & 7)) * 16))
+                                 : "memory");
+                tmem_st32(tmem + lane_off + kTmemQ + (4u * hf + bq) * 32u, v);
             }
             if (hf) {
-                const uint32_t qr = sm.base + kOffQR + row_off;
+                const uint32_t pr = us + (uint32_t)(q4 >> 1);  // heads 0-63: first stage, 64-127: second
+                if (pr != pc) MLA_WAIT_WARP(sm.bar(kBarFull + pr % kStagesS), (pr / kStagesS) & 1u, abort);
+                const uint32_t src = sm.stage(pr % kStagesS, kStageS) + kQRopeOff + (uint32_t)(h & 63) * 128u;
+                uint32_t v[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 x = __ldg(q + 8 * 8 + u);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qr + (uint32_t)((u ^ (h & 7)) * 16)),
-                                 "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                                 : "r"(src + (uint32_t)((c ^ (lane & 7)) * 16))
                                  : "memory");
-                }
-                fence_proxy_async_smem();  // generic writes -> the MMAs (async proxy)
+                tmem_st32(tmem + lane_off + kTmemQR, v);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarQReady));
+            us += 2u + (uint32_t)(it.te - it.tb);
         }
         // l: the row sum of the unrounded probabilities (for the lse); lr: the sum of the bf16
         // probabilities the PV product actually uses, which normalises O -- numerator and
@@ -577,28 +658,40 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
         float m = 0.f, l = 0.f, lr = 0.f, lt = 0.f, lrt = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
             const uint32_t buf = sc & 1u;
-#pragma unroll
-            for (int t = 0; t < kIssuers; ++t) MLA_WAIT_WARP(sm.bar(kBarSFull + 2 * t + (int)buf), (sc >> 1) & 1u, abort);
+            MLA_WAIT_WARP(sm.bar(kBarSFull + (int)buf), (sc >> 1) & 1u, abort);
             tc_fence_after();
-            float s[32];
+            // this thread's half of the row, and the other half for the row maximum only: both
+            // threads of a head then take the same maximum (fmaxf is exact and order-free)
+            // without exchanging anything
+            const int vrow = min(kPage, it.n_vis - tile * kPage);  // valid columns of the page
+            float s[32], omx;
             {
                 uint32_t a[32], b[32];
-                tmem_ld32(tmem + lane_off + kTmemS + buf * 128u + 32u * hf, a);
-                tmem_ld32(tmem + lane_off + kTmemS + buf * 128u + 64u + 32u * hf, b);
-                tmem_ld_wait();
+                tmem_ld32(tmem + lane_off + kTmemS + buf * 64u + 32u * hf, a);
+                tmem_ld32(tmem + lane_off + kTmemS + buf * 64u + 32u * (1 - hf), b);
+                tmem_ld_wait_dep(a);
+                tmem_ld_wait_dep(b);
+                const int vo = vrow - 32 * (1 - hf);
+                float m4[4];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(a[c]) + __uint_as_float(b[c]);
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    float x = 8 * g4 < vo ? __uint_as_float(b[8 * g4]) : -INFINITY;
+#pragma unroll
+                    for (int c = 1; c < 8; ++c) x = 8 * g4 + c < vo ? fmaxf(x, __uint_as_float(b[8 * g4 + c])) : x;
+                    m4[g4] = x;
+                }
+                omx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+#pragma unroll
+                for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(a[c]);
             }
             tc_fence_before();
             mbar_arrive(sm.bar(kBarSEmpty + (int)buf));
 
-            const int valid = min(kPage, it.n_vis - tile * kPage) - 32 * hf;  // columns of this half
+            const int valid = vrow - 32 * hf;  // columns of this half
             if (valid < 32) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) s[c] = c < valid ? s[c] : -INFINITY;
             }
-            // row max: this half as a tree (fmaxf is exact, so the order does not matter), then
-            // the partner's half through shared memory (double-buffered by page parity)
             float mx4[4];
 #pragma unroll
             for (int g4 = 0; g4 < 4; ++g4) {
@@ -608,15 +701,6 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 mx4[g4] = a;
             }
             const float lmx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            const uint32_t xb = xmax + (sc & 1u) * (2u * kHeads * 4u);
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(xb + (uint32_t)(hf * kHeads + h) * 4u), "f"(lmx) : "memory");
-            {  // both warps of the quadrant have written (a bounded wait, unlike a named barrier)
-                const uint32_t xbar = sm.bar(kBarXMax + 2 * q4 + (int)(sc & 1u));
-                mbar_arrive(xbar);
-                MLA_WAIT_WARP(xbar, (sc >> 1) & 1u, abort);
-            }
-            float omx;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(omx) : "r"(xb + (uint32_t)((1 - hf) * kHeads + h) * 4u) : "memory");
             const float mx = fmaxf(lmx, omx) * sl2;
             const bool first = tile == it.tb;
             const bool last = tile == it.te - 1;
@@ -664,11 +748,20 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             const uint32_t rs = sc % kRing;
             MLA_WAIT_WARP(sm.bar(kBarPFree + rs), ((sc / kRing) & 1u) ^ 1u, abort);
             uint8_t *msg = ring + (size_t)rs * kMsgBytes;
+            // chunks 2v and 2v + 1 of this half-row land in one aligned 32-byte sector (the swizzle
+            // flips the low bit of the chunk index, or not): one 32-byte store per pair
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = 4 * hf + u;
-                st_global_v4_hint(msg + row_off + (uint32_t)((c ^ (h & 7)) * 16),
-                                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]), keep);
+            for (int v = 0; v < 2; ++v) {
+                const uint32_t p0 = (uint32_t)((4 * hf + 2 * v) ^ (h & 7));
+                const bool swap = (p0 & 1u) != 0;
+                uint32_t w8[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w8[i] = swap ? pk[8 * v + 4 + i] : pk[8 * v + i];
+                    w8[4 + i] = swap ? pk[8 * v + i] : pk[8 * v + 4 + i];
+                }
+                st_global_v8_hint(msg + row_off + (p0 & ~1u) * 16u, w8[0], w8[1], w8[2], w8[3], w8[4], w8[5], w8[6],
+                                  w8[7], keep);
             }
             if (hf == 0) {
                 st_global_f32_hint(msg + kPBytes + 4u * h, alpha, keep);
@@ -687,43 +780,43 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
     }
 }
 
-// Score CTA, shippers (one thread each, kShippers of them): publish the ring slots the
-// softmax warps have written to the partner, kBatch at a time, with one cluster-scope release
-// per batch; shipper j handles the batches b with b % kShippers == j.  A shipper acquires the
-// rows through the local barrier, and release/acquire chains are transitive, so the partner's
-// acquire sees every row.  Such a release waits for the rows' stores to complete and costs
-// about a microsecond here: batching and several shippers keep that off the page rate, and
-// the compute warps never touch a cluster-scope barrier.
-static_assert(kRing % kBatch == 0 && kRingBatches >= 3, "ring must hold at least three batches");
-__device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, uint32_t me, int cid, int ncl,
-                                             int n_items, volatile int *abort) {
+// Score CTA, shipper (one thread): publishes the messages the softmax warps have written to
+// the partner.  It waits for the oldest unpublished message, takes the later ones of the same
+// item that are already complete (up to kMaxBatch), and publishes them together: one
+// cluster-scope release fence, then a relaxed remote arrival per message.  The fence waits
+// for the rows' stores to complete and costs about a microsecond here, so messages that pile
+// up meanwhile share the next one, while a message that comes alone (an item's first and
+// last pages) goes out at once.  The shipper acquired the rows through the local barriers
+// and the fence is cumulative, so the partner's acquire sees every row.
+__device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, const Sched &sc,
+                                             volatile int *abort) {
     uint32_t g = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
-        for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            if ((g / kBatch) % kShippers != me) continue;
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
+        const uint32_t end = g + (uint32_t)(it.te > it.tb ? it.te - it.tb : 0);
+        while (g < end) {
             if (!mbar_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
-            if ((g + 1) % kBatch == 0)
-                mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
+            uint32_t n = 1;
+            while (g + n < end && n < (uint32_t)kMaxBatch &&
+                   mbar_test(sm.bar(kBarPStaged + (g + n) % kRing), ((g + n) / kRing) & 1u))
+                ++n;
+            fence_acq_rel_cluster();
+            for (uint32_t k = 0; k < n; ++k)
+                mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPReady + (g + k) % kRing), 1));
+            g += n;
         }
     }
-    if (g % kBatch != 0 && (g / kBatch) % kShippers == me)  // the last, partial batch
-        mbar_arrive_cluster(mapa_shared(sm.bar(kBarPReady + (g / kBatch) % kRingBatches), 1));
 }
 
 // Accumulate CTA, releaser (one thread): hands each ring slot back to the partner as soon as
 // its message has landed in shared memory, off the MMA warp's path.  Its local arrival is
 // the second one each P buffer needs before the loader refills it, so this thread can never
 // fall a whole buffer cycle behind the barrier it watches.
-__device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
+__device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem &sm, const Sched &sc,
                                               volatile int *abort) {
     uint32_t g = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             if (!mbar_wait(sm.bar(kBarPFull + g % kPBufs), (g / kPBufs) & 1u, abort)) return;
             mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPFree + g % kRing), 0));
@@ -733,28 +826,23 @@ __device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem 
 }
 
 // Accumulate CTA, P loader (one thread): ring slot -> shared P buffer, as soon as the
-// partner has written it and the buffer's previous message has been used.
-__device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, int cid, int ncl, int n_items,
+// partner has published it and the buffer's previous message has been used.
+__device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, const Sched &sc,
                                               volatile int *abort) {
-    const uint8_t *ring = p.ring + (size_t)cid * kRing * kMsgBytes;
+    const uint8_t *ring = p.ring + (size_t)sc.cid * kRing * kMsgBytes;
     const uint64_t keep = l2_policy_evict_last();
     uint32_t g = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             const uint32_t rs = g % kRing, jp = g % kPBufs;
-            if (g % kBatch == 0) {  // a new batch: wait until the partner has published it
-                const uint32_t b = g / kBatch;
-                if (!mbar_wait<true>(sm.bar(kBarPReady + b % kRingBatches), (b / kRingBatches) & 1u, abort)) return;
-                fence_proxy_async_global();  // the partner's writes, before our async-proxy reads
-            }
+            if (!mbar_wait<true>(sm.bar(kBarPReady + rs), (g / kRing) & 1u, abort)) return;
+            fence_proxy_async_global();  // the partner's writes, before our async-proxy reads
             if (!mbar_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
             mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
-            const uint8_t *msg = ring + (size_t)rs * kMsgBytes;
-            bulk_load_g2s(sm.pbuf(jp), msg, kPBytes, sm.bar(kBarPFull + jp), keep);
-            bulk_load_g2s(sm.meta(jp), msg + kPBytes, kMetaBytes, sm.bar(kBarPFull + jp), keep);
+            // P and its factors are contiguous in both places: one copy (the copy engine's cost
+            // per transfer is high)
+            bulk_load_g2s(sm.pbuf(jp), ring + (size_t)rs * kMsgBytes, kMsgBytes, sm.bar(kBarPFull + jp), keep);
         }
     }
 }
@@ -763,16 +851,15 @@ __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem 
 // hands rescale and epilogue events to the epilogue warps through the local event buffer:
 // the event data is written, then the event barrier gets two arrivals -- this warp's
 // (release: the data is visible) and the MMA commit (all earlier MMAs have completed).
-__device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, int cid,
-                                               int ncl, int n_items, volatile int *abort) {
+__device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+                                               volatile int *abort) {
     const int lane = threadIdx.x & 31;
     uint32_t g = 0, cv = 0;
     bool pending_epilogue = false;
+    uint32_t staging_buf = 0;  // P buffer the epilogue warps are writing the output through
     const uint32_t evt = sm.evt();
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             const uint32_t jp = g % kPBufs;
             const bool first = tile == it.tb, last = tile == it.te - 1;
@@ -784,6 +871,7 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                     if (!warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
                     ++cv;
                     pending_epilogue = false;
+                    if (lane == 0) mbar_arrive(sm.bar(kBarPBufFree + staging_buf));  // staging done
                 }
             } else {
                 float4 a4;
@@ -809,36 +897,39 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                 }
             }
             const uint64_t a0 = sdesc_sw128(sm.pbuf(jp), 16u, 1024u);
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const uint32_t u = 2u * g + n, s = u % kStagesV;
-                if (!warp_wait(sm.bar(kBarFull + s), (u / kStagesV) & 1u, abort)) return;
-                const uint32_t vb = sm.stage(s, kStageV);
-                if (last && valid < (uint32_t)kPage) {
-                    // rows past the end of the sequence may hold anything (even NaN): zero them,
-                    // since 0 * NaN would poison O even though their probabilities are 0
-                    const uint32_t nrow = kPage - valid;
-                    for (uint32_t e = lane; e < nrow * 8u * (kBoxesV / 2); e += 32) {
-                        uint32_t bx = e / (nrow * 8u), rem = e % (nrow * 8u);
-                        uint32_t row = valid + rem / 8u, ch = rem % 8u;
-                        uint32_t addr = vb + bx * kBoxBytes + row * 128u + ch * 16u;
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+            const uint32_t s = g % kStagesV;
+            if (!warp_wait(sm.bar(kBarFull + s), (g / kStagesV) & 1u, abort)) return;
+            const uint32_t vb = sm.stage(s, kStageV);
+            if (last && valid < (uint32_t)kPage) {
+                // rows past the end of the sequence may hold anything (even NaN): zero them,
+                // since 0 * NaN would poison O even though their probabilities are 0
+                const uint32_t nrow = kPage - valid;
+                for (uint32_t e = lane; e < nrow * 8u * kBoxesV; e += 32) {
+                    const uint32_t bx = e / (nrow * 8u), rem = e % (nrow * 8u);
+                    const uint32_t row = valid + rem / 8u, ch = rem % 8u;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + bx * kBoxBytes + row * 128u +
+                                                                                   ch * 16u),
+                                 "r"(0u)
+                                 : "memory");
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t v0 = sdesc_sw128(vb, (uint32_t)kBoxBytes, 1024u);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const uint64_t v0 = sdesc_sw128(vb + (uint32_t)n * 4u * kBoxBytes, (uint32_t)kBoxBytes, 1024u);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_ss(tmem + 256u * n, a0 + (uint64_t)((32u * k) >> 4), v0 + (uint64_t)((2048u * k) >> 4),
                                kIdescPV, !(first && k == 0));
-                    mma_commit(sm.bar(kBarEmpty + s));
-                    if (n == 1) mma_commit(sm.bar(kBarPBufFree + jp));
                 }
-                __syncwarp();
+                mma_commit(sm.bar(kBarEmpty + s));
+                // an item's last P buffer is released after the epilogue has used it
+                if (!last) mma_commit(sm.bar(kBarPBufFree + jp));
             }
+            __syncwarp();
             if (last) {
                 // epilogue event: 1/l per head to the event buffer
                 asm volatile("{\n\t.reg .b32 x, y, z, w;\n\t"
@@ -849,10 +940,12 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
                 __syncwarp();
                 if (lane == 0) {
                     asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1024u), "r"(kEvtEpilogue) : "memory");
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(evt + 1028u), "r"(jp) : "memory");
                     mbar_arrive(sm.bar(kBarMmaEvt));
                     mma_commit(sm.bar(kBarMmaEvt));
                 }
                 pending_epilogue = true;
+                staging_buf = jp;
             }
             __syncwarp();
         }
@@ -863,18 +956,43 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
 // Accumulate CTA, epilogue warps.  Eight warps: warp w owns heads 32(w%4) .. +31 (its TMEM
 // lane quadrant) and latent columns [256 hf, 256 hf + 256), hf = w / 4.  They serve events --
 // rescale their part of the O rows, or write the normalised output of the finished item.
+// A thread holds one row of O, so the output goes through shared memory (2 KB per warp, in
+// the item's last P buffer, whose MMAs have completed): each thread stages 64 bytes of its row,
+// then each store instruction writes 64 contiguous bytes of 8 rows instead of 16 bytes of 32.
+// The staged 16-byte chunks are rotated by row so that neither side has bank conflicts.
+__device__ __forceinline__ void stage_and_store(uint32_t stg, int lane, const uint32_t (&v)[16], uint8_t *row0,
+                                                size_t row_bytes) {
+    const uint32_t rot = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + (uint32_t)lane * 64u +
+                                                                     (((uint32_t)k ^ rot) * 16u)),
+                     "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                     : "memory");
+    __syncwarp();
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+        const uint32_t rr = 8u * s4 + ((uint32_t)lane >> 2), j = (uint32_t)lane & 3u;
+        uint4 x;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                     : "r"(stg + rr * 64u + ((j ^ ((rr >> 1) & 3u)) * 16u))
+                     : "memory");
+        *reinterpret_cast<uint4 *>(row0 + rr * row_bytes + j * 16u) = x;
+    }
+    __syncwarp();
+}
+
 __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const Smem &sm, uint32_t tmem,
-                                                    int cid, int ncl, int n_items, volatile int *abort) {
-    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2;
-    const int h = q4 * 32 + (threadIdx.x & 31);
+                                                    const Sched &sc, volatile int *abort) {
+    const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2, lane = threadIdx.x & 31;
+    const int h = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t col0 = 256u * hf;
     const uint32_t evt = sm.evt();
     uint32_t ev = 0;
-    for (int r = 0;; ++r) {
-        const int i = schedule(r, cid, ncl);
-        if (i >= n_items) break;
-        const ItemInfo it = load_item(p, i);
+    ItemInfo it;
+    for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) {
             uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + col0);
             for (int c = 0; c < 256 * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
@@ -894,7 +1012,7 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
                     for (int c = 0; c < 8; ++c) {
                         uint32_t v[32];
                         tmem_ld32(tmem + lane_off + col0 + c * 32u, v);
-                        tmem_ld_wait();
+                        tmem_ld_wait_dep(v);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                         tmem_st32(tmem + lane_off + col0 + c * 32u, v);
@@ -906,31 +1024,43 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
                 continue;
             }
             float inv_l;
+            uint32_t jp;
             asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv_l) : "r"(evt + 512u + 4u * h) : "memory");
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + col0 + c * 32u, v);
-                tmem_ld_wait();
-                if (it.slot < 0) {
-                    uint4 *o = reinterpret_cast<uint4 *>(p.o_lat + ((size_t)it.bt * kHeads + h) * kDc + col0 + c * 32);
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(jp) : "r"(evt + 1028u) : "memory");
+            const uint32_t stg = sm.pbuf(jp) + (uint32_t)w * 2048u;
+            // each chunk's TMEM load is issued before the previous chunk is stored
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col0, v);
+            if (it.slot < 0) {
+                uint8_t *row0 = reinterpret_cast<uint8_t *>(p.o_lat + ((size_t)it.bt * kHeads + q4 * 32) * kDc + col0);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 q;
-                        q.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv_l, __uint_as_float(v[8 * u + 1]) * inv_l);
-                        q.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv_l, __uint_as_float(v[8 * u + 3]) * inv_l);
-                        q.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv_l, __uint_as_float(v[8 * u + 5]) * inv_l);
-                        q.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv_l, __uint_as_float(v[8 * u + 7]) * inv_l);
-                        o[u] = q;
+                for (int c = 0; c < 8; ++c) {
+                    tmem_ld_wait_dep(v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+                    if (c + 1 < 8) tmem_ld32(tmem + lane_off + col0 + (c + 1) * 32u, v);
+                    stage_and_store(stg, lane, pk, row0 + c * 64, (size_t)kDc * 2);
+                }
+            } else {
+                uint8_t *row0 = reinterpret_cast<uint8_t *>(p.part_o + ((size_t)it.slot * kHeads + q4 * 32) * kDc + col0);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    tmem_ld_wait_dep(v);
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        lo[e] = __float_as_uint(__uint_as_float(v[e]) * inv_l);
+                        hi[e] = __float_as_uint(__uint_as_float(v[16 + e]) * inv_l);
                     }
-                } else {
-                    float4 *o = reinterpret_cast<float4 *>(p.part_o + ((size_t)it.slot * kHeads + h) * kDc + col0 + c * 32);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        o[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
-                                           __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
+                    if (c + 1 < 8) tmem_ld32(tmem + lane_off + col0 + (c + 1) * 32u, v);
+                    stage_and_store(stg, lane, lo, row0 + c * 128, (size_t)kDc * 4);
+                    stage_and_store(stg, lane, hi, row0 + c * 128 + 64, (size_t)kDc * 4);
                 }
             }
+            // the staging writes (generic proxy) before the loader's next bulk copy into the buffer
+            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarCorrEvt));
             break;
@@ -939,11 +1069,12 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
 }
 
 // Launched with a cluster dimension of 2 (rank 0 scores, rank 1 accumulates), 13 warps:
-// 0-7 softmax (rank 0) / epilogue (rank 1), 8 page producer, 9-11 the three score MMA issuers
-// (rank 0) / the PV MMA warp, the P loader and the ring-slot releaser (rank 1), 12 the
-// message shipper (rank 0).
+// 0-7 softmax (rank 0) / epilogue (rank 1), 8 page producer, 9-10 the two score MMA
+// issuers (rank 0) / 9-11 the PV MMA warp, the P loader and the ring-slot releaser (rank 1),
+// 12 the message shipper (rank 0).
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_v,
+              const __grid_constant__ CUtensorMap tmap_qc, const __grid_constant__ CUtensorMap tmap_qr,
               const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -951,7 +1082,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     sm.base = (raw + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
     const uint32_t rank = cluster_ctarank();
-    const int cid = (int)cluster_id_x(), ncl = (int)nclusters_x();
     uint8_t *const gbase = smem_raw + (sm.base - raw);
     volatile int *abort = reinterpret_cast<volatile int *>(gbase + kOffAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemPtr);
@@ -959,21 +1089,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesMax; ++s) {
             mbar_init(sm.bar(kBarFull + s), 1);
-            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? kIssuers : 1);  // score: every issuer commits
+            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? kIssuers : 1);  // score: both issuers commit
         }
-        for (int j = 0; j < 2 * kIssuers; ++j) mbar_init(sm.bar(kBarSFull + j), 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(sm.bar(kBarSHalf + j), 1);  // issuer 0's commit
+            mbar_init(sm.bar(kBarSFull + j), 1);  // issuer 1's commit
+        }
         for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSEmpty + j), 256);  // every softmax thread
         mbar_init(sm.bar(kBarQReady), 256);
-        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPFree + j), 1);  // score CTA: the partner's releaser
-        for (int j = 0; j < kRingBatches; ++j) mbar_init(sm.bar(kBarPReady + j), 1);  // accumulate CTA: the shipper
-        for (int j = 0; j < kRing; ++j) mbar_init(sm.bar(kBarPStaged + j), 256);  // score CTA: softmax threads
+        for (int j = 0; j < kRing; ++j) {
+            mbar_init(sm.bar(kBarPFree + j), 1);     // score CTA: the partner's releaser
+            mbar_init(sm.bar(kBarPReady + j), 1);    // accumulate CTA: the partner's shipper
+            mbar_init(sm.bar(kBarPStaged + j), 256); // score CTA: softmax threads
+        }
         for (int j = 0; j < kPBufs; ++j) {
             mbar_init(sm.bar(kBarPFull + j), 1);     // accumulate CTA: armed by the P loader
-            mbar_init(sm.bar(kBarPBufFree + j), 2);  // accumulate CTA: MMA commit + releaser
+            mbar_init(sm.bar(kBarPBufFree + j), 2);  // accumulate CTA: MMA commit (or epilogue done) + releaser
         }
         mbar_init(sm.bar(kBarMmaEvt), 2);            // MMA warp arrive + MMA commit
         mbar_init(sm.bar(kBarCorrEvt), 256);  // every epilogue thread
-        for (int j = 0; j < 12; ++j) mbar_init(sm.bar(kBarXMax + j), 64);  // the two warps of a quadrant
+        for (int j = 0; j < 4; ++j) mbar_init(sm.bar(kBarXSum + j), 64);  // the two warps of a quadrant
         *abort = 0;
         fence_mbar_init();
     }
@@ -981,7 +1116,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
         tmem_alloc(sm.base + kOffTmemPtr, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kWarpProducer && (threadIdx.x & 31) == 0) tma_prefetch_desc(rank == 0 ? &tmap_s : &tmap_v);
+    if (warp == kWarpProducer && (threadIdx.x & 31) == 0) {
+        if (rank == 0) {
+            tma_prefetch_desc(&tmap_s);
+            tma_prefetch_desc(&tmap_qc);
+            tma_prefetch_desc(&tmap_qr);
+        } else {
+            tma_prefetch_desc(&tmap_v);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // the partner's barriers exist before any remote arrive
@@ -991,32 +1134,36 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     // the plan's results are read only after it has completed
     grid_dependency_wait();
     grid_launch_dependents();  // let the combine kernel's blocks get resident early
-    const int n_items = p.hdr->n_items;
+    Sched sc;
+    sc.cid = (int)cluster_id_x();
+    sc.ncl = (int)nclusters_x();
+    sc.n_items = p.hdr->n_items;
+    sc.first = load_item(p, sc.cid < p.max_items ? sc.cid : 0);  // needed only if cid < n_items
 
     const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp < 8) {
         if (rank == 0)
-            role_softmax(p, sm, tmem, cid, ncl, n_items, abort);
+            role_softmax(p, sm, tmem, sc, abort);
         else
-            role_accum_epilogue(p, sm, tmem, cid, ncl, n_items, abort);
+            role_accum_epilogue(p, sm, tmem, sc, abort);
     } else if (warp == kWarpProducer) {
         if (rank == 0)
-            role_producer<kStagesS, 1>(p, &tmap_s, sm, kStageS, true, cid, ncl, n_items, abort);
+            role_score_producer(p, &tmap_s, &tmap_qc, &tmap_qr, sm, sc, abort);
         else
-            role_producer<kStagesV, 2>(p, &tmap_v, sm, kStageV, false, cid, ncl, n_items, abort);
+            role_value_producer(p, &tmap_v, sm, sc, abort);
     } else if (warp < kWarpMma + 3) {
         if (rank == 0) {
-            if (warp < kWarpMma + kIssuers && lane0)
-                role_score_mma(p, sm, tmem, (uint32_t)(warp - kWarpMma), cid, ncl, n_items, abort);
+            if (warp == kWarpMma && lane0) role_score_mma<0>(p, sm, tmem, sc, abort);
+            if (warp == kWarpMma + 1 && lane0) role_score_mma<1>(p, sm, tmem, sc, abort);
         } else if (warp == kWarpMma) {
-            role_accum_mma(p, sm, tmem, cid, ncl, n_items, abort);
+            role_accum_mma(p, sm, tmem, sc, abort);
         } else if (warp == kWarpMma + 1) {
-            if (lane0) role_p_loader(p, sm, cid, ncl, n_items, abort);
+            if (lane0) role_p_loader(p, sm, sc, abort);
         } else {
-            if (lane0) role_releaser(p, sm, cid, ncl, n_items, abort);
+            if (lane0) role_releaser(p, sm, sc, abort);
         }
-    } else if (warp >= kWarpShipper) {
-        if (rank == 0 && lane0) role_shipper(p, sm, (uint32_t)(warp - kWarpShipper), cid, ncl, n_items, abort);
+    } else if (warp == kWarpShipper) {
+        if (rank == 0 && lane0) role_shipper(p, sm, sc, abort);
     }
 
     tc_fence_before();

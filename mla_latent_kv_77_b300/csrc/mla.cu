@@ -112,52 +112,53 @@ bool tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
-// 3-D view of the latent page pool for whole-page TMA loads: (64 columns, rows, 9 column
-// blocks) with strides (2 B, 1152 B, 128 B).  A box of (64, 64, blocks) is one page's
-// first `blocks` 64-column blocks, landing as consecutive 8 KB swizzled blocks.
-bool tmap_pool_pages(CUtensorMap *m, const void *pool, uint64_t num_pages, uint32_t blocks) {
-    cuuint64_t dims[3] = {64, num_pages * kPage, (cuuint64_t)kBoxesS};
+// 3-D view of a [rows, 576] bf16 array (the latent page pool, or the absorbed queries) for TMA:
+// (64 columns, rows, 9 column blocks) with strides (2 B, 1152 B, 128 B).  A box of
+// (64, box_rows, blocks) lands as `blocks` consecutive box_rows x 128-byte swizzled blocks.
+bool tmap_row_blocks(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows, uint32_t blocks) {
+    cuuint64_t dims[3] = {64, rows, (cuuint64_t)kBoxesS};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kPage, blocks};
+    cuuint32_t box[3] = {64, box_rows, blocks};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// Pool tensor maps are encoded once per (device, pool, pages, blocks) and reused: a decode
-// step of a serving loop sees the same pool every call.
-struct PoolMapEntry {
+// Tensor maps are encoded once per (device, array, rows, box) and reused: a decode step of a
+// serving loop sees the same pool every call, and often the same query buffer.
+struct MapEntry {
     int dev;
-    const void *pool;
-    uint64_t num_pages;
-    uint32_t blocks;
+    const void *base;
+    uint64_t rows;
+    uint32_t box_rows, blocks;
     CUtensorMap map;
 };
-constexpr int kPoolMapCache = 16;
-PoolMapEntry g_pool_maps[kPoolMapCache];
-int g_pool_maps_n = 0, g_pool_maps_next = 0;
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+int g_maps_n = 0, g_maps_next = 0;
 std::mutex g_map_mu;
 
-bool pool_map_cached(CUtensorMap *m, int dev, const void *pool, uint64_t num_pages, uint32_t blocks) {
+bool map_cached(CUtensorMap *m, int dev, const void *base, uint64_t rows, uint32_t box_rows, uint32_t blocks) {
     std::lock_guard<std::mutex> lk(g_map_mu);
-    for (int i = 0; i < g_pool_maps_n; ++i) {
-        const PoolMapEntry &e = g_pool_maps[i];
-        if (e.dev == dev && e.pool == pool && e.num_pages == num_pages && e.blocks == blocks) {
+    for (int i = 0; i < g_maps_n; ++i) {
+        const MapEntry &e = g_maps[i];
+        if (e.dev == dev && e.base == base && e.rows == rows && e.box_rows == box_rows && e.blocks == blocks) {
             *m = e.map;
             return true;
         }
     }
-    if (!tmap_pool_pages(m, pool, num_pages, blocks)) return false;
-    PoolMapEntry &e = g_pool_maps[g_pool_maps_next];
+    if (!tmap_row_blocks(m, base, rows, box_rows, blocks)) return false;
+    MapEntry &e = g_maps[g_maps_next];
     e.dev = dev;
-    e.pool = pool;
-    e.num_pages = num_pages;
+    e.base = base;
+    e.rows = rows;
+    e.box_rows = box_rows;
     e.blocks = blocks;
     e.map = *m;
-    g_pool_maps_next = (g_pool_maps_next + 1) % kPoolMapCache;
-    if (g_pool_maps_n < kPoolMapCache) ++g_pool_maps_n;
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    if (g_maps_n < kMapCache) ++g_maps_n;
     return true;
 }
 
@@ -327,9 +328,13 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
 
-    CUtensorMap tmap_s, tmap_v;
-    if (!pool_map_cached(&tmap_s, dev, kv_pool, (uint64_t)num_pages, kBoxesS) ||
-        !pool_map_cached(&tmap_v, dev, kv_pool, (uint64_t)num_pages, kBoxesV / 2))
+    // pages: all 9 column blocks (score stage) or the 8 latent blocks (value stage) of one page;
+    // queries: 4 content blocks of all 128 heads, or the RoPE block of 64 heads
+    const uint64_t pool_rows = (uint64_t)num_pages * kPage, q_rows = (uint64_t)batch * q_len * kHeads;
+    CUtensorMap tmap_s, tmap_v, tmap_qc, tmap_qr;
+    if (!map_cached(&tmap_s, dev, kv_pool, pool_rows, kPage, kBoxesS) ||
+        !map_cached(&tmap_v, dev, kv_pool, pool_rows, kPage, kBoxesV) ||
+        !map_cached(&tmap_qc, dev, q_abs, q_rows, kHeads, 4) || !map_cached(&tmap_qr, dev, q_abs, q_rows, 64, 1))
         return MLA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -360,6 +365,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     p.causal = causal ? 1 : 0;
     p.num_pages = num_pages;
     p.max_pages = max_pages;
+    p.max_items = w.max_items;
     p.sl2 = scale * 1.4426950408889634f;
 
     cudaLaunchConfig_t cfg = {};
@@ -378,7 +384,7 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, tmap_qc, tmap_qr, p) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
