@@ -6,21 +6,18 @@
 // stays in latent space, o = sum_j softmax(s)_j c_j (W^UV is applied later).
 //
 // B300 design: one cluster of two CTAs (two SMs) per work item.
-//   CTA rank 0, the "score" CTA: holds the 128x576 absorbed query of the item as
-//     the MMA A operand (content part in tensor memory, RoPE part in shared
-//     memory), streams the 64-token pages with one
-//     3-D TMA per page into a 2-stage ring (L2 is asked to keep each page for
-//     the partner's second read),
-//     and computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05.
-//     Two MMA warps split each page's K range (column blocks 0-3, and 4-7 plus
-//     the RoPE block 8) into two partial S tiles -- one thread cannot issue
-//     N = 64 MMAs fast enough to keep the tensor pipe busy, two can -- and the
-//     partial tiles are double-buffered, so the next page's MMAs run while the
-//     softmax warps read this one's.  That fits because the query's content part
-//     (256 columns) sits in TMEM and its RoPE part in shared memory.  Eight
-//     softmax warps add the partials, run the online softmax with lazy
-//     rescaling and write P (bf16, 128 x 64) plus per-head factors straight from
-//     registers into a ring of messages in global memory (it stays in L2).
+//   CTA rank 0, the "score" CTA: streams the 64-token pages with one 3-D TMA box per page
+//     into three page stages (L2 is asked to keep each page for the partner's second
+//     read); the item's absorbed query (128 x 576) first passes through two stage
+//     positions and is copied into tensor memory, where it is the MMA A operand.  It
+//     computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05: one thread
+//     cannot issue N = 64 MMAs fast enough to keep the tensor pipe busy, so two issuers
+//     share each page -- the second accumulates the RoPE block and blocks 4-7 onto the
+//     tile once the first has done blocks 0-3 -- and S is double-buffered in TMEM, so the
+//     next page's MMAs run while the softmax warps read this one's.  Eight softmax warps
+//     run the online softmax with lazy rescaling and write P (bf16, 128 x 64) plus
+//     per-head factors straight from registers into a ring of messages in global memory
+//     (it stays in L2).
 //   CTA rank 1, the "accumulate" CTA: holds O = 128 heads x 512 latent fp32, i.e.
 //     all 512 TMEM columns, streams the same pages' 512 latent columns (L2 hits:
 //     the score CTA has just pulled them from HBM), bulk-copies each P message
