@@ -547,43 +547,52 @@ __device__ __forceinline__ void role_score_producer(const DecodeParams &p, const
 template <int kMe>
 __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
                                                volatile int *abort) {
+    // the whole warp runs the loop, so the descriptors stay warp-uniform values; one lane
+    // issues the MMAs and commits
+    const bool leader = (threadIdx.x & 31) == 0;
     uint32_t g = 0, ic = 0, u = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) continue;
-        if (!mbar_wait(sm.bar(kBarQReady), ic & 1u, abort)) return;
+        MLA_WAIT_WARP(sm.bar(kBarQReady), ic & 1u, abort);
         tc_fence_after();
         ++ic;
-        mbar_arrive(sm.bar(kBarEmpty + u % kStagesS));
-        mbar_arrive(sm.bar(kBarEmpty + (u + 1) % kStagesS));
+        if (leader) {
+            mbar_arrive(sm.bar(kBarEmpty + u % kStagesS));
+            mbar_arrive(sm.bar(kBarEmpty + (u + 1) % kStagesS));
+        }
+        __syncwarp();
         u += 2;
         for (int tile = it.tb; tile < it.te; ++tile, ++g, ++u) {
             const uint32_t s = u % kStagesS, buf = g & 1u;
-            if (!mbar_wait(sm.bar(kBarFull + s), (u / kStagesS) & 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarFull + s), (u / kStagesS) & 1u, abort);
             if (kMe == 0) {
-                if (!mbar_wait(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort)) return;
+                MLA_WAIT_WARP(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort);
             } else {
-                if (!mbar_wait(sm.bar(kBarSHalf + (int)buf), (g >> 1) & 1u, abort)) return;
+                MLA_WAIT_WARP(sm.bar(kBarSHalf + (int)buf), (g >> 1) & 1u, abort);
             }
             tc_fence_after();
             const uint32_t d = tmem + kTmemS + buf * 64u;
             const uint32_t a0 = tmem + kTmemQ + kMe * 4u * 32u;
             const uint32_t st = sm.stage(s, kStageS);
             const uint64_t b0 = sdesc_sw128(st + kMe * 4u * kBoxBytes, 16u, 1024u);
+            if (leader) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
-                mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS,
-                       kMe == 1 || k != 0);
-            }
-            if (kMe == 1) {  // the RoPE block
-                const uint64_t br = sdesc_sw128(st + 8u * kBoxBytes, 16u, 1024u);
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
+                    mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS,
+                           kMe == 1 || k != 0);
+                }
+                if (kMe == 1) {  // the RoPE block
+                    const uint64_t br = sdesc_sw128(st + 8u * kBoxBytes, 16u, 1024u);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(d, tmem + kTmemQR + kk * 8u, br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(d, tmem + kTmemQR + kk * 8u, br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
+                }
+                mma_commit(sm.bar(kBarEmpty + s));
+                mma_commit(sm.bar((kMe == 0 ? kBarSHalf : kBarSFull) + (int)buf));
             }
-            mma_commit(sm.bar(kBarEmpty + s));
-            mma_commit(sm.bar((kMe == 0 ? kBarSHalf : kBarSFull) + (int)buf));
+            __syncwarp();
         }
     }
 }
@@ -1150,8 +1159,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
             role_value_producer(p, &tmap_v, sm, sc, abort);
     } else if (warp < kWarpMma + 3) {
         if (rank == 0) {
-            if (warp == kWarpMma && lane0) role_score_mma<0>(p, sm, tmem, sc, abort);
-            if (warp == kWarpMma + 1 && lane0) role_score_mma<1>(p, sm, tmem, sc, abort);
+            if (warp == kWarpMma) role_score_mma<0>(p, sm, tmem, sc, abort);
+            if (warp == kWarpMma + 1) role_score_mma<1>(p, sm, tmem, sc, abort);
         } else if (warp == kWarpMma) {
             role_accum_mma(p, sm, tmem, sc, abort);
         } else if (warp == kWarpMma + 1) {
