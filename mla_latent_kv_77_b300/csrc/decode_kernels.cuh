@@ -12,9 +12,8 @@
 //     positions and is copied into tensor memory, where it is the MMA A operand.  It
 //     computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05: one thread
 //     cannot issue N = 64 MMAs fast enough to keep the tensor pipe busy, so two issuers
-//     share each page -- the second accumulates the RoPE block and blocks 4-7 onto the
-//     tile once the first has done blocks 0-3 -- and S is double-buffered in TMEM, so the
-//     next page's MMAs run while the softmax warps read this one's.  Eight softmax warps
+//     take alternate pages, each into its own S buffer in TMEM; the next page's MMAs run
+//     while the softmax warps read this one's.  Eight softmax warps
 //     run the online softmax with lazy rescaling and write P (bf16, 128 x 64) plus
 //     per-head factors straight from registers into a ring of messages in global memory
 //     (it stays in L2).
@@ -60,7 +59,6 @@ constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (fact
 constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns
-constexpr int kIssuers = 2;          // score CTA MMA issuers: column blocks 0-3 | 4-7 and the RoPE block 8
 constexpr uint32_t kTmemS = 0;       // score CTA: S tile of buffer b at 64 b
 constexpr uint32_t kTmemQR = 128;    // score CTA: Q RoPE part (block 8, bf16 pairs) at 128 .. 159
 constexpr uint32_t kTmemQ = 256;     // score CTA: Q content part (blocks 0-7, bf16 pairs) at 256 .. 511
@@ -78,11 +76,12 @@ constexpr uint32_t kOffBar = kScoreEnd > kAccumEnd ? kScoreEnd : kAccumEnd;
 constexpr int kStagesMax = kStagesS > kStagesV ? kStagesS : kStagesV;
 constexpr int kBarFull = 0;                          // page stages
 constexpr int kBarEmpty = kBarFull + kStagesMax;
-constexpr int kBarSHalf = kBarEmpty + kStagesMax;    // score: issuer 0's part of S tile [buffer] done
-constexpr int kBarSFull = kBarSHalf + 2;             // score: S tile [buffer] complete
+constexpr int kBarSFull = kBarEmpty + kStagesMax;    // score: S tile [buffer] complete
 constexpr int kBarSEmpty = kBarSFull + 2;            // score: S tile [buffer] read by the softmax warps
-constexpr int kBarQReady = kBarSEmpty + 2;           // score: the item's Q is in TMEM and shared memory
-constexpr int kBarPFree = kBarQReady + 1;            // score: ring slot consumed (partner arrives)
+constexpr int kBarQReady = kBarSEmpty + 2;           // score: the item's Q is in TMEM
+constexpr int kBarQAck = kBarQReady + 1;             // score: both issuers have seen the item's QReady
+constexpr int kBarDrain = kBarQAck + 1;              // MMA warps: all of a warp's MMAs done [warp], at exit
+constexpr int kBarPFree = kBarDrain + 2;             // score: ring slot consumed (partner arrives)
 constexpr int kBarPReady = kBarPFree + kRing;        // accumulate: a ring slot written (partner arrives)
 constexpr int kBarPStaged = kBarPReady + kRing;      // score: all rows of a ring slot written
 constexpr int kBarPFull = kBarPStaged + kRing;       // accumulate: P buffer landed
@@ -465,11 +464,19 @@ struct PageIds {
 // map views the pool as (64 columns, rows, 9 column blocks) with strides (2 B, 1152 B, 128 B),
 // so a box lands as consecutive 64-row x 128-byte swizzled blocks -- the MMAs' operand layout.
 // These reads are a page's second: L2 may drop the lines afterwards (evict_first).
-__device__ __forceinline__ void role_value_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort) {
+// The loops below return the number of stage positions whose loads they issued; the role then
+// drains the last of them (normal exit or abort), so no copy lands after the CTA has moved on.
+__device__ __forceinline__ void drain_stages(const Smem &sm, uint32_t issued, uint32_t stages) {
+    if ((threadIdx.x & 31) == 0)
+        for (uint32_t k = (issued > stages ? issued - stages : 0); k < issued; ++k)
+            if (!mbar_wait_drain(sm.bar(kBarFull + k % stages), (k / stages) & 1u)) break;
+    __syncwarp();
+}
+
+__device__ __forceinline__ void value_producer_loop(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
+                                                    const Sched &sc, volatile int *abort, uint32_t &u) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = l2_policy_evict_first();
-    uint32_t u = 0;
     ItemInfo it;
     PageIds ids;
     for (int r = 0; sc.get(p, r, it); ++r) {
@@ -485,10 +492,12 @@ __device__ __forceinline__ void role_value_producer(const DecodeParams &p, const
             __syncwarp();
         }
     }
-    // let every load issued land before the CTA can retire (bounded)
-    if (lane == 0)
-        for (uint32_t k = (u > kStagesV ? u - kStagesV : 0); k < u; ++k)
-            if (!mbar_wait(sm.bar(kBarFull + k % kStagesV), (k / kStagesV) & 1u, abort)) return;
+}
+__device__ __forceinline__ void role_value_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
+                                                    const Sched &sc, volatile int *abort) {
+    uint32_t u = 0;
+    value_producer_loop(p, tmap, sm, sc, abort, u);
+    drain_stages(sm, u, kStagesV);
 }
 
 // Score CTA, page producer (a whole warp; lane 0 issues).  Its stage sequence holds, per item,
@@ -497,12 +506,11 @@ __device__ __forceinline__ void role_value_producer(const DecodeParams &p, const
 // two stages of its positions -- and then one whole page per position.  Every transfer is one
 // large box (the TMA engine's cost per box is high).  Pages are read first here: L2 keeps them for
 // the partner (evict_last); the query is read once (evict_first).
-__device__ __forceinline__ void role_score_producer(const DecodeParams &p, const CUtensorMap *pages,
+__device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const CUtensorMap *pages,
                                                     const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort) {
+                                                    const Sched &sc, volatile int *abort, uint32_t &u) {
     const int lane = threadIdx.x & 31;
     const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
-    uint32_t u = 0;
     ItemInfo it;
     PageIds ids;
     for (int r = 0; sc.get(p, r, it); ++r) {
@@ -531,24 +539,28 @@ __device__ __forceinline__ void role_score_producer(const DecodeParams &p, const
             __syncwarp();
         }
     }
-    // let every load issued land before the CTA can retire (bounded)
-    if (lane == 0)
-        for (uint32_t k = (u > kStagesS ? u - kStagesS : 0); k < u; ++k)
-            if (!mbar_wait(sm.bar(kBarFull + k % kStagesS), (k / kStagesS) & 1u, abort)) return;
+}
+__device__ __forceinline__ void role_score_producer(const DecodeParams &p, const CUtensorMap *pages,
+                                                    const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
+                                                    const Sched &sc, volatile int *abort) {
+    uint32_t u = 0;
+    score_producer_loop(p, pages, qc, qr, sm, sc, abort, u);
+    drain_stages(sm, u, kStagesS);
 }
 
-// Score CTA, MMA issuer kMe (one thread each).  One thread cannot issue N = 64 MMAs fast enough
-// to keep the tensor pipe busy, two can: issuer 0 computes column blocks 0-3 of S = Q . K_tile^T
-// into the page's S tile, and issuer 1, once that part has completed, accumulates blocks 4-7 and
-// the RoPE block 8 onto it (A from TMEM throughout).  Page g uses S buffer g & 1, so issuer 0
-// works on page g + 1 while issuer 1 finishes page g.  A stage is free once both have committed.
-// The two query stages are handed back (one plain arrival each) once the softmax warps report
-// the query in TMEM.
+// Score CTA, MMA issuer warp kMe.  One thread cannot issue N = 64 MMAs fast enough to keep the
+// tensor pipe busy; two can.  The issuers take alternate pages -- page g goes to issuer g & 1 and
+// into S buffer g & 1 -- and each computes the whole S = Q . K_tile^T of its pages (column blocks
+// 0-7 and the RoPE block 8, A from TMEM), so the pipe sees two independent streams.  Both
+// issuers still walk every stage position in order: the page's issuer commits its MMAs to the
+// stage's empty barrier and the other one adds a plain arrival once the page has landed, so a
+// stage is refilled only after both have passed it -- a parity wait can then never see its
+// barrier a phase behind or two phases ahead.  Both hand the two query stages back (one plain
+// arrival each) once the softmax warps report the query in TMEM.  The whole warp runs the loop,
+// so the descriptors stay warp-uniform values; one lane issues the MMAs and commits.
 template <int kMe>
-__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+__device__ __forceinline__ void score_mma_loop(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
                                                volatile int *abort) {
-    // the whole warp runs the loop, so the descriptors stay warp-uniform values; one lane
-    // issues the MMAs and commits
     const bool leader = (threadIdx.x & 31) == 0;
     uint32_t g = 0, ic = 0, u = 0;
     ItemInfo it;
@@ -557,44 +569,58 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
         MLA_WAIT_WARP(sm.bar(kBarQReady), ic & 1u, abort);
         tc_fence_after();
         ++ic;
+        // acknowledge: the softmax warps complete the next item's QReady only after both issuers
+        // have seen this one, so an issuer with no page in an item cannot fall two phases behind
         if (leader) {
+            mbar_arrive(sm.bar(kBarQAck));
             mbar_arrive(sm.bar(kBarEmpty + u % kStagesS));
             mbar_arrive(sm.bar(kBarEmpty + (u + 1) % kStagesS));
         }
         __syncwarp();
         u += 2;
         for (int tile = it.tb; tile < it.te; ++tile, ++g, ++u) {
-            const uint32_t s = u % kStagesS, buf = g & 1u;
+            const uint32_t s = u % kStagesS, buf = (uint32_t)kMe;
+            // every position is waited for in order, so no parity wait can run ahead of its
+            // barrier; a position of the other issuer's page only gets this warp's release
             MLA_WAIT_WARP(sm.bar(kBarFull + s), (u / kStagesS) & 1u, abort);
-            if (kMe == 0) {
-                MLA_WAIT_WARP(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort);
-            } else {
-                MLA_WAIT_WARP(sm.bar(kBarSHalf + (int)buf), (g >> 1) & 1u, abort);
+            if ((g & 1u) != (uint32_t)kMe) {
+                if (leader) mbar_arrive(sm.bar(kBarEmpty + s));
+                __syncwarp();
+                continue;
             }
+            MLA_WAIT_WARP(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort);
             tc_fence_after();
             const uint32_t d = tmem + kTmemS + buf * 64u;
-            const uint32_t a0 = tmem + kTmemQ + kMe * 4u * 32u;
             const uint32_t st = sm.stage(s, kStageS);
-            const uint64_t b0 = sdesc_sw128(st + kMe * 4u * kBoxBytes, 16u, 1024u);
+            const uint64_t b0 = sdesc_sw128(st, 16u, 1024u);
             if (leader) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
+                for (int k = 0; k < 32; ++k) {
                     const uint32_t bx = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
-                    mma_ts(d, a0 + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4), kIdescS,
-                           kMe == 1 || k != 0);
+                    mma_ts(d, tmem + kTmemQ + bx * 32u + kk * 8u, b0 + (uint64_t)((bx * kBoxBytes + kk * 32u) >> 4),
+                           kIdescS, k != 0);
                 }
-                if (kMe == 1) {  // the RoPE block
-                    const uint64_t br = sdesc_sw128(st + 8u * kBoxBytes, 16u, 1024u);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(d, tmem + kTmemQR + kk * 8u, br + (uint64_t)((32u * kk) >> 4), kIdescS, 1u);
-                }
+                for (int kk = 0; kk < 4; ++kk)  // the RoPE block
+                    mma_ts(d, tmem + kTmemQR + kk * 8u, b0 + (uint64_t)((8u * kBoxBytes + 32u * kk) >> 4), kIdescS, 1u);
                 mma_commit(sm.bar(kBarEmpty + s));
-                mma_commit(sm.bar((kMe == 0 ? kBarSHalf : kBarSFull) + (int)buf));
+                mma_commit(sm.bar(kBarSFull + (int)buf));
             }
             __syncwarp();
         }
     }
+}
+// On any exit, normal or after an abort, every MMA this warp issued has completed before the
+// CTA can free its tensor memory: a final commit, waited for with the abort-ignoring bound.
+template <int kMe>
+__device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+                                               volatile int *abort) {
+    score_mma_loop<kMe>(p, sm, tmem, sc, abort);
+    if ((threadIdx.x & 31) == 0) {
+        mma_commit(sm.bar(kBarDrain + kMe));
+        mbar_wait_drain(sm.bar(kBarDrain + kMe), 0);
+    }
+    __syncwarp();
 }
 
 // Score CTA, softmax warps.  Eight warps, two per sub-partition: warp w owns heads
@@ -621,6 +647,9 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             if (hf == 0) p.lse[(size_t)it.bt * kHeads + h] = -INFINITY;
             continue;
         }
+        // both issuers have seen the previous item's QReady before this item's can complete
+        // (nsum counts the items finished so far)
+        if (nsum > 0) MLA_WAIT_WARP(sm.bar(kBarQAck), (nsum - 1u) & 1u, abort);
         // this head's absorbed query, from the item's two query stages (the previous item's MMAs
         // are done: its last S tile has been read): content blocks 4 hf .. 4 hf + 3 -> TMEM lane h
         // (bf16 pairs), and for hf = 1 the RoPE block -> TMEM lane h too.  Both stages hold
@@ -833,11 +862,10 @@ __device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem 
 
 // Accumulate CTA, P loader (one thread): ring slot -> shared P buffer, as soon as the
 // partner has published it and the buffer's previous message has been used.
-__device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, const Sched &sc,
-                                              volatile int *abort) {
+__device__ __forceinline__ void p_loader_loop(const DecodeParams &p, const Smem &sm, const Sched &sc,
+                                              volatile int *abort, uint32_t &g) {
     const uint8_t *ring = p.ring + (size_t)sc.cid * kRing * kMsgBytes;
     const uint64_t keep = l2_policy_evict_last();
-    uint32_t g = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
@@ -852,12 +880,20 @@ __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem 
         }
     }
 }
+// the copies issued last may still be in flight after an abort: wait for them (bounded)
+__device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, const Sched &sc,
+                                              volatile int *abort) {
+    uint32_t g = 0;
+    p_loader_loop(p, sm, sc, abort, g);
+    for (uint32_t k = (g > (uint32_t)kPBufs ? g - kPBufs : 0); k < g; ++k)
+        if (!mbar_wait_drain(sm.bar(kBarPFull + k % kPBufs), (k / kPBufs) & 1u)) break;
+}
 
 // Accumulate CTA, MMA warp: O += P V, two N = 256 halves, K = 64 in 4 steps.  It also
 // hands rescale and epilogue events to the epilogue warps through the local event buffer:
 // the event data is written, then the event barrier gets two arrivals -- this warp's
 // (release: the data is visible) and the MMA commit (all earlier MMAs have completed).
-__device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+__device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
                                                volatile int *abort) {
     const int lane = threadIdx.x & 31;
     uint32_t g = 0, cv = 0;
@@ -957,6 +993,16 @@ __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem
         }
     }
     if (pending_epilogue) warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort);
+}
+// every MMA this warp issued has completed before the CTA can free its tensor memory
+__device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
+                                               volatile int *abort) {
+    accum_mma_loop(p, sm, tmem, sc, abort);
+    if ((threadIdx.x & 31) == 0) {
+        mma_commit(sm.bar(kBarDrain));
+        mbar_wait_drain(sm.bar(kBarDrain), 0);
+    }
+    __syncwarp();
 }
 
 // Accumulate CTA, epilogue warps.  Eight warps: warp w owns heads 32(w%4) .. +31 (its TMEM
@@ -1095,14 +1141,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesMax; ++s) {
             mbar_init(sm.bar(kBarFull + s), 1);
-            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? kIssuers : 1);  // score: both issuers commit
+            // score: the page's issuer commits and the other issuer arrives (both arrive for a
+            // query stage); accumulate: the PV MMA commit
+            mbar_init(sm.bar(kBarEmpty + s), rank == 0 ? 2 : 1);
         }
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(sm.bar(kBarSHalf + j), 1);  // issuer 0's commit
-            mbar_init(sm.bar(kBarSFull + j), 1);  // issuer 1's commit
-        }
+        for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSFull + j), 1);  // the page's issuer commits
         for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarSEmpty + j), 256);  // every softmax thread
         mbar_init(sm.bar(kBarQReady), 256);
+        mbar_init(sm.bar(kBarQAck), 2);             // each score issuer, once per item
+        for (int j = 0; j < 2; ++j) mbar_init(sm.bar(kBarDrain + j), 1);
         for (int j = 0; j < kRing; ++j) {
             mbar_init(sm.bar(kBarPFree + j), 1);     // score CTA: the partner's releaser
             mbar_init(sm.bar(kBarPReady + j), 1);    // accumulate CTA: the partner's shipper
@@ -1172,6 +1219,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
         if (rank == 0 && lane0) role_shipper(p, sm, sc, abort);
     }
 
+    // every thread's own tensor-memory loads and stores have completed (they may be in flight
+    // when a role left early after an abort)
+    tmem_ld_wait();
+    tmem_st_wait();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // neither CTA retires while its partner may still arrive on it

@@ -135,6 +135,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Bounded wait that ignores the abort flag: after an abort, a role still waits for the copies
+// and MMAs it has already issued (they complete within microseconds) before the CTA may free
+// its tensor memory or exit.  Gives up after 10 ms.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 10000000ull) {
+            raise_status(0x4u);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch
 // ----------------------------------------------------------------------------
