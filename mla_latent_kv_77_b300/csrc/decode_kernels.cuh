@@ -7,8 +7,8 @@
 //
 // B300 design: one cluster of two CTAs (two SMs) per work item.
 //   CTA rank 0, the "score" CTA: streams the 64-token pages with one 3-D TMA box per page
-//     into three page stages (L2 is asked to keep each page for the partner's second
-//     read); the item's absorbed query (128 x 576) first passes through two stage
+//     into three page stages (the partner re-reads each page from L2 shortly after); the
+//     item's absorbed query (128 x 576) first passes through two stage
 //     positions and is copied into tensor memory, where it is the MMA A operand.  It
 //     computes S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) with tcgen05: one thread
 //     cannot issue N = 64 MMAs fast enough to keep the tensor pipe busy, so two issuers
@@ -365,11 +365,18 @@ struct Smem {
 };
 
 // L2 eviction policies.  Every page is read twice, by the score CTA and microseconds later by
-// its partner: the first read asks L2 to keep the lines (evict_last), the second lets them go
-// (evict_first).  The P ring is rewritten in place and should never leave L2 (evict_last).
+// its partner: the first read uses the normal priority, the second lets the lines go
+// (evict_first) -- measured faster than asking L2 to keep them on the first read (evict_last),
+// which crowds the working set.  The P ring is rewritten in place and should never leave L2
+// (evict_last).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -504,13 +511,13 @@ __device__ __forceinline__ void role_value_producer(const DecodeParams &p, const
 // first the absorbed query -- position 0: column blocks 0-3 of all heads and the RoPE block of
 // heads 0-63; position 1: blocks 4-7 and the RoPE block of heads 64-127, which exactly fills the
 // two stages of its positions -- and then one whole page per position.  Every transfer is one
-// large box (the TMA engine's cost per box is high).  Pages are read first here: L2 keeps them for
-// the partner (evict_last); the query is read once (evict_first).
+// large box (the TMA engine's cost per box is high).  Pages are read first here, at the normal
+// L2 priority (the partner's second read lets them go); the query is read once (evict_first).
 __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const CUtensorMap *pages,
                                                     const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
                                                     const Sched &sc, volatile int *abort, uint32_t &u) {
     const int lane = threadIdx.x & 31;
-    const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+    const uint64_t keep = l2_policy_evict_normal(), once = l2_policy_evict_first();
     ItemInfo it;
     PageIds ids;
     for (int r = 0; sc.get(p, r, it); ++r) {
