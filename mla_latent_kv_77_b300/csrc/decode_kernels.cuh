@@ -401,11 +401,6 @@ __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uin
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
-__device__ __forceinline__ void st_global_v4_hint(void *dst, uint4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w), "l"(pol)
-                 : "memory");
-}
 __device__ __forceinline__ void st_global_v8_hint(void *dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
                                                   uint32_t f, uint32_t g, uint32_t h, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst), "r"(a),

@@ -68,11 +68,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// arrive on a barrier of another CTA of the cluster (cluster_bar from mapa_shared)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -166,22 +161,6 @@ __device__ __forceinline__ void grid_launch_dependents() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-// barrier among nthreads that also ORs a predicate across them
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %3, 0;\n\t"
-        "bar.red.or.pred po, %1, %2, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"(id), "r"(nthreads), "r"((uint32_t)pred)
-        : "memory");
-    return out != 0;
-}
 
 // ----------------------------------------------------------------------------
 // TMA (tiled tensor loads) and bulk copies
@@ -195,16 +174,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void *tmap,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-// shared::cta -> shared::cluster (another CTA), completion counted on a barrier of the
-// destination CTA (dst and bar are shared::cluster addresses).
-__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                              uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst_cluster),
-        "r"(src_cta), "r"(bytes), "r"(bar_cluster)
         : "memory");
 }
 
@@ -254,14 +223,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-// same, arriving on the barrier at the same offset in every CTA of `cta_mask`
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
