@@ -232,7 +232,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
     __shared__ int s_arr[4 * kPlanSmemBt];
     const int tid = threadIdx.x;
     const int n_bt = B * Tq;
-    const int per = (n_bt + kPlanThreads - 1) / kPlanThreads;
+    const int nthr = (int)blockDim.x;  // up to kPlanThreads; the host launches as few as the batch needs
+    const int per = (n_bt + nthr - 1) / nthr;
     int *const base = n_bt <= kPlanSmemBt ? s_arr : scratch;
     const int stride = n_bt <= kPlanSmemBt ? kPlanSmemBt : n_bt;
     int *const tiles = base, *const splits = base + stride, *const slot_base = base + 2 * stride,
@@ -277,7 +278,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
     __syncthreads();
 
     // 3. order: longest chunk first (rank sort when it fits one element per thread)
-    const bool sorted = n_bt <= kPlanThreads;
+    const bool sorted = n_bt <= nthr;
     if (sorted) {
         int key = -1;
         if (tid < n_bt) {

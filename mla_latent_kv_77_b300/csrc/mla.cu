@@ -344,7 +344,10 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     const int n_bt = batch * q_len;
     cudaStream_t s = (cudaStream_t)stream;
 
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
+    // one thread per query up to kPlanThreads (the rank sort wants that), in whole warps, at
+    // least four: a small batch plans with few threads and few warps to synchronise
+    const int plan_threads = n_bt >= kPlanThreads ? kPlanThreads : (n_bt <= 128 ? 128 : (n_bt + 31) / 32 * 32);
+    plan_kernel<<<1, plan_threads, 0, s>>>(seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
                                            num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch),
                                            w.max_items, w.max_slots);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
