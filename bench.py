@@ -128,6 +128,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value, on every rank (x itself with one rank): the job's time is
+    that of its slowest replica."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_step: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_step * steps * world / (slowest_ms / 1000.0)
+
+
 def cpu_oracle_rate(case, budget_s: float = 12.0, max_seqs: int = None):
     """Time the fp64 oracle (absorbed form, all host cores) on a bounded sample of whole
     sequences of the workload; returns (tokens/s, cores, sample description)."""
@@ -260,16 +277,12 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     st, word = mla.get_device_status()
     assert st == 0, f"device status {word:#x}"
 
     tokens_per_step = B * Tq
-    value = tokens_per_step * args.steps * world / (total_ms / 1000.0)
+    value = job_rate(tokens_per_step, args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
     cache_bytes = int(case.seq_lens.to(torch.int64).sum()) * ROW_BYTES
     vis = case.seq_lens.to(torch.int64)
@@ -312,12 +325,8 @@ def main():
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens_per_step * args.steps * world / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_rate(tokens_per_step, args.steps, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
