@@ -51,7 +51,7 @@ constexpr uint32_t kStageV = kBoxesV * kBoxBytes;  // 65536: a page's 512 latent
 constexpr int kStagesV = 2;          // accumulate CTA page stages
 constexpr int kPBufs = 4;            // accumulate CTA: P messages held in shared memory
 constexpr int kRing = 16;            // P messages in flight through global memory, per CTA pair
-constexpr int kMaxBatch = 4;         // messages published together (one cluster-scope release each)
+constexpr int kMaxBatch = 4;         // most messages published behind one cluster-scope fence
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
 constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one message: P, then its factors
