@@ -64,19 +64,79 @@ def profiled_traffic(workload: str):
     return e.get("dram_bytes_per_launch")
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+class _Nvml:
+    """The few NVML calls the sampler needs, through ctypes on the driver's libnvidia-ml
+    (read-only queries)."""
 
+    CLOCK_SM = 1
+
+    def __init__(self, index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            raise RuntimeError("no NVML device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn) -> float:
+        v = self.c.c_uint()
+        if fn(self.dev, self.c.c_int(self.CLOCK_SM), self.c.byref(v)) != 0:
+            raise RuntimeError("NVML clock query failed")
+        return float(v.value)
+
+    def sm_clock(self) -> float:
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def sm_max_clock(self) -> float:
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reasons(self) -> int:
+        v = self.c.c_ulonglong()
+        if self.reasons_fn(self.dev, self.c.byref(v)) != 0:
+            raise RuntimeError("NVML reasons query failed")
+        return int(v.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clock and throttle reasons sampled during the timed region (read only).
+
+    NVML is polled from a background thread about every millisecond, so even a timed region
+    of a few milliseconds holds samples; only those between mark_begin() and mark_end() are
+    reported.  Without NVML it falls back to nvidia-smi at 100 ms (whose samples then mostly
+    fall outside a short timed region; `source` says which was used)."""
+
+    # NVML clock-event reason bits
+    REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40))
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, gpu_index: int, period_s: float = 0.001):
+        self.gpu, self.period = gpu_index, period_s
+        self.nv = self.proc = None
+        self.samples, self.t_begin, self.t_end = [], None, None
         self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        try:
+            import threading
+            self.nv = _Nvml(self.gpu)
+            self.smax = self.nv.sm_max_clock()
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            time.sleep(0.02)
+            return self
+        except Exception:
+            self.nv = None
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -87,7 +147,29 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            try:
+                t = time.perf_counter()
+                self.samples.append((t, self.nv.sm_clock(), self.nv.reasons()))
+            except Exception:
+                return
+            time.sleep(self.period)
+
+    def mark_begin(self):
+        self.t_begin = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+
     def __exit__(self, *a):
+        if self.nv is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            try:
+                self.nv.close()
+            except Exception:
+                pass
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -97,8 +179,20 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        if self.nv is not None:
+            lo = self.t_begin if self.t_begin is not None else -math.inf
+            hi = self.t_end if self.t_end is not None else math.inf
+            win = [x for x in self.samples if lo <= x[0] <= hi]
+            reasons = set()
+            for _, _, rs in win:
+                for name, bit in self.REASONS:
+                    if rs & bit:
+                        reasons.add(name)
+            sm = [x[1] for x in win]
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.smax,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, about 1 ms, timed region only"}
         if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         sm, smax, reasons = [], None, set()
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
@@ -118,7 +212,7 @@ class ClockSampler:
         except OSError:
             pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 100 ms"}
 
 
 def dist_setup():
@@ -270,11 +364,13 @@ def main():
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        clk.mark_begin()
         t_start.record(stream)
         for i in range(args.steps):
             step(i)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if world > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
