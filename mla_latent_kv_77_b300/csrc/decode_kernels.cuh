@@ -477,7 +477,7 @@ __device__ __forceinline__ void drain_stages(const Smem &sm, uint32_t issued, ui
 }
 
 __device__ __forceinline__ void value_producer_loop(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort, uint32_t &u) {
+                                                    const Sched &sc, volatile int *abort, uint32_t &u, Tracer &tr) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = l2_policy_evict_first();
     ItemInfo it;
@@ -487,19 +487,21 @@ __device__ __forceinline__ void value_producer_loop(const DecodeParams &p, const
         for (int tile = it.tb; tile < it.te; ++tile, ++u) {
             const int pg = ids.get(p, it, tile, lane);
             const uint32_t s = u % kStagesV;
+            tr.at(0x50);
             if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesV) & 1u) ^ 1u, abort)) return;
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageV);
                 tma_load_3d(sm.stage(s, kStageV), tmap, 0, pg * kPage, 0, sm.bar(kBarFull + s), pol);
             }
+            tr.at(0x51);
             __syncwarp();
         }
     }
 }
 __device__ __forceinline__ void role_value_producer(const DecodeParams &p, const CUtensorMap *tmap, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort) {
+                                                    const Sched &sc, volatile int *abort, Tracer &tr) {
     uint32_t u = 0;
-    value_producer_loop(p, tmap, sm, sc, abort, u);
+    value_producer_loop(p, tmap, sm, sc, abort, u, tr);
     drain_stages(sm, u, kStagesV);
 }
 
@@ -511,18 +513,19 @@ __device__ __forceinline__ void role_value_producer(const DecodeParams &p, const
 // L2 priority (the partner's second read lets them go); the query is read once (evict_first).
 __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const CUtensorMap *pages,
                                                     const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort, uint32_t &u) {
+                                                    const Sched &sc, volatile int *abort, uint32_t &u, Tracer &tr) {
     const int lane = threadIdx.x & 31;
     const uint64_t keep = l2_policy_evict_normal(), once = l2_policy_evict_first();
     ItemInfo it;
     PageIds ids;
     for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) continue;
-        ids.start(p, it, lane);
         const int row0 = it.bt * kHeads;
         for (int hq = 0; hq < 2; ++hq, ++u) {
             const uint32_t s = u % kStagesS;
+            tr.at(0x12);
             if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            tr.at(0x13);
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
                 tma_load_3d(sm.stage(s, kStageS), qc, 0, row0, 4 * hq, sm.bar(kBarFull + s), once);
@@ -531,10 +534,13 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
             }
             __syncwarp();
         }
+        ids.start(p, it, lane);  // the block table is read once the query's loads are on their way
         for (int tile = it.tb; tile < it.te; ++tile, ++u) {
             const int pg = ids.get(p, it, tile, lane);
             const uint32_t s = u % kStagesS;
+            tr.at(0x10);
             if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            tr.at(0x11);
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
                 tma_load_3d(sm.stage(s, kStageS), pages, 0, pg * kPage, 0, sm.bar(kBarFull + s), keep);
@@ -545,9 +551,9 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
 }
 __device__ __forceinline__ void role_score_producer(const DecodeParams &p, const CUtensorMap *pages,
                                                     const CUtensorMap *qc, const CUtensorMap *qr, const Smem &sm,
-                                                    const Sched &sc, volatile int *abort) {
+                                                    const Sched &sc, volatile int *abort, Tracer &tr) {
     uint32_t u = 0;
-    score_producer_loop(p, pages, qc, qr, sm, sc, abort, u);
+    score_producer_loop(p, pages, qc, qr, sm, sc, abort, u, tr);
     drain_stages(sm, u, kStagesS);
 }
 
@@ -563,13 +569,15 @@ __device__ __forceinline__ void role_score_producer(const DecodeParams &p, const
 // so the descriptors stay warp-uniform values; one lane issues the MMAs and commits.
 template <int kMe>
 __device__ __forceinline__ void score_mma_loop(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
-                                               volatile int *abort) {
+                                               volatile int *abort, Tracer &tr) {
     const bool leader = (threadIdx.x & 31) == 0;
     uint32_t g = 0, ic = 0, u = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) continue;
+        tr.at(0x20);
         MLA_WAIT_WARP(sm.bar(kBarQReady), ic & 1u, abort);
+        tr.at(0x21);
         tc_fence_after();
         ++ic;
         // acknowledge: the softmax warps complete the next item's QReady only after both issuers
@@ -585,13 +593,17 @@ __device__ __forceinline__ void score_mma_loop(const DecodeParams &p, const Smem
             const uint32_t s = u % kStagesS, buf = (uint32_t)kMe;
             // every position is waited for in order, so no parity wait can run ahead of its
             // barrier; a position of the other issuer's page only gets this warp's release
+            tr.at(0x22);
             MLA_WAIT_WARP(sm.bar(kBarFull + s), (u / kStagesS) & 1u, abort);
             if ((g & 1u) != (uint32_t)kMe) {
+                tr.at(0x24);
                 if (leader) mbar_arrive(sm.bar(kBarEmpty + s));
                 __syncwarp();
                 continue;
             }
+            tr.at(0x23);
             MLA_WAIT_WARP(sm.bar(kBarSEmpty + (int)buf), ((g >> 1) & 1u) ^ 1u, abort);
+            tr.at(0x25);
             tc_fence_after();
             const uint32_t d = tmem + kTmemS + buf * 64u;
             const uint32_t st = sm.stage(s, kStageS);
@@ -609,6 +621,7 @@ __device__ __forceinline__ void score_mma_loop(const DecodeParams &p, const Smem
                 mma_commit(sm.bar(kBarEmpty + s));
                 mma_commit(sm.bar(kBarSFull + (int)buf));
             }
+            tr.at(0x26);
             __syncwarp();
         }
     }
@@ -617,8 +630,8 @@ __device__ __forceinline__ void score_mma_loop(const DecodeParams &p, const Smem
 // CTA can free its tensor memory: a final commit, waited for with the abort-ignoring bound.
 template <int kMe>
 __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
-                                               volatile int *abort) {
-    score_mma_loop<kMe>(p, sm, tmem, sc, abort);
+                                               volatile int *abort, Tracer &tr) {
+    score_mma_loop<kMe>(p, sm, tmem, sc, abort, tr);
     if ((threadIdx.x & 31) == 0) {
         mma_commit(sm.bar(kBarDrain + kMe));
         mbar_wait_drain(sm.bar(kBarDrain + kMe), 0);
@@ -634,7 +647,7 @@ __device__ __forceinline__ void role_score_mma(const DecodeParams &p, const Smem
 // half-row of the P message (bf16 in the UMMA K-major 128-byte-swizzle image, the rescale factor,
 // and 1/l on the item's last page) into the ring, then signal the shipper.
 __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &scd,
-                                             volatile int *abort) {
+                                             volatile int *abort, Tracer &tr) {
     const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2, lane = threadIdx.x & 31;
     const int h = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -644,6 +657,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
     const uint32_t xsum = sm.base + kOffXSum;
     const uint64_t keep = l2_policy_evict_last();
     uint32_t sc = 0, nsum = 0, us = 0;
+    int staged_pending = -1;  // ring slot whose message is written but not yet released to the shipper
     ItemInfo it;
     for (int r = 0; scd.get(p, r, it); ++r) {
         if (it.te <= it.tb) {
@@ -652,6 +666,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
         }
         // both issuers have seen the previous item's QReady before this item's can complete
         // (nsum counts the items finished so far)
+        tr.at(0x30);
         if (nsum > 0) MLA_WAIT_WARP(sm.bar(kBarQAck), (nsum - 1u) & 1u, abort);
         // this head's absorbed query, from the item's two query stages (the previous item's MMAs
         // are done: its last S tile has been read): content blocks 4 hf .. 4 hf + 3 -> TMEM lane h
@@ -688,6 +703,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarQReady));
+            tr.at(0x31);
             us += 2u + (uint32_t)(it.te - it.tb);
         }
         // l: the row sum of the unrounded probabilities (for the lse); lr: the sum of the bf16
@@ -696,7 +712,9 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
         float m = 0.f, l = 0.f, lr = 0.f, lt = 0.f, lrt = 0.f;
         for (int tile = it.tb; tile < it.te; ++tile, ++sc) {
             const uint32_t buf = sc & 1u;
+            tr.at(0x32);
             MLA_WAIT_WARP(sm.bar(kBarSFull + (int)buf), (sc >> 1) & 1u, abort);
+            tr.at(0x33);
             tc_fence_after();
             // this thread's half of the row, and the other half for the row maximum only: both
             // threads of a head then take the same maximum (fmaxf is exact and order-free)
@@ -710,35 +728,42 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 tmem_ld_wait_dep(a);
                 tmem_ld_wait_dep(b);
                 const int vo = vrow - 32 * (1 - hf);
-                float m4[4];
+                if (vo >= 32) {
+                    omx = fmax3(fmax3(__uint_as_float(b[0]), __uint_as_float(b[1]), __uint_as_float(b[2])),
+                                fmax3(__uint_as_float(b[3]), __uint_as_float(b[4]), __uint_as_float(b[5])),
+                                __uint_as_float(b[6]));
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    float x = 8 * g4 < vo ? __uint_as_float(b[8 * g4]) : -INFINITY;
+                    for (int c = 7; c < 31; c += 2)
+                        omx = fmax3(omx, __uint_as_float(b[c]), __uint_as_float(b[c + 1]));
+                    omx = fmaxf(omx, __uint_as_float(b[31]));
+                } else {  // the page's ragged tail
+                    omx = -INFINITY;
 #pragma unroll
-                    for (int c = 1; c < 8; ++c) x = 8 * g4 + c < vo ? fmaxf(x, __uint_as_float(b[8 * g4 + c])) : x;
-                    m4[g4] = x;
+                    for (int c = 0; c < 32; ++c) omx = c < vo ? fmaxf(omx, __uint_as_float(b[c])) : omx;
                 }
-                omx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 #pragma unroll
                 for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(a[c]);
             }
             tc_fence_before();
             mbar_arrive(sm.bar(kBarSEmpty + (int)buf));
+            tr.at(0x34);
+            // the previous page's message, whose stores have had a page's time to complete, is
+            // released to the shipper now rather than right after them (the release would wait
+            // for them)
+            if (staged_pending >= 0) {
+                mbar_arrive(sm.bar(kBarPStaged + staged_pending));
+                staged_pending = -1;
+            }
 
             const int valid = vrow - 32 * hf;  // columns of this half
             if (valid < 32) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) s[c] = c < valid ? s[c] : -INFINITY;
             }
-            float mx4[4];
+            float lmx = fmax3(fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), s[6]);
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-                float a = s[8 * g4];
-#pragma unroll
-                for (int c = 1; c < 8; ++c) a = fmaxf(a, s[8 * g4 + c]);
-                mx4[g4] = a;
-            }
-            const float lmx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            for (int c = 7; c < 31; c += 2) lmx = fmax3(lmx, s[c], s[c + 1]);
+            lmx = fmaxf(lmx, s[31]);
             const float mx = fmaxf(lmx, omx) * sl2;
             const bool first = tile == it.tb;
             const bool last = tile == it.te - 1;
@@ -751,18 +776,27 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 lr *= alpha;
                 m = mx;
             }
+            // p = 2^(s sl2 - m) on pairs: one paired FMA, two exponentials, one bf16 pair; the two
+            // row sums on pairs too
             uint32_t pk[16];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f}, lsr[2] = {0.f, 0.f};
+            uint64_t ls2[2] = {0ull, 0ull}, lr2[2] = {0ull, 0ull};
+            const uint64_t sl2x2 = f32x2(sl2, sl2), nmx2 = f32x2(-m, -m);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float a = ex2_approx(fmaf(s[2 * c], sl2, -m));
-                const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
+                float y0, y1;
+                f32x2_split(fma_f32x2(f32x2(s[2 * c], s[2 * c + 1]), sl2x2, nmx2), y0, y1);
+                const float a = ex2_approx(y0), b = ex2_approx(y1);
                 pk[c] = pack_bf16x2(a, b);
-                ls[c & 3] += a + b;
-                lsr[c & 1] += bf16lo_to_f32(pk[c]) + bf16hi_to_f32(pk[c]);
+                ls2[c & 1] = add_f32x2(ls2[c & 1], f32x2(a, b));
+                lr2[c & 1] = add_f32x2(lr2[c & 1], f32x2(bf16lo_to_f32(pk[c]), bf16hi_to_f32(pk[c])));
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            lr += lsr[0] + lsr[1];
+            {
+                float a0, a1, b0, b1;
+                f32x2_split(add_f32x2(ls2[0], ls2[1]), a0, a1);
+                f32x2_split(add_f32x2(lr2[0], lr2[1]), b0, b1);
+                l += a0 + a1;
+                lr += b0 + b1;
+            }
             if (last) {  // the whole row's sums, for 1/l and the lse
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + (uint32_t)(hf * kHeads + h) * 4u), "f"(l) : "memory");
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + (uint32_t)((2 + hf) * kHeads + h) * 4u), "f"(lr)
@@ -784,7 +818,9 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
             // arrived): this half-row of P in the UMMA K-major 128-byte-swizzle image, the
             // rescale factor, and 1/l on the item's last page
             const uint32_t rs = sc % kRing;
+            tr.at(0x35);
             MLA_WAIT_WARP(sm.bar(kBarPFree + rs), ((sc / kRing) & 1u) ^ 1u, abort);
+            tr.at(0x36);
             uint8_t *msg = ring + (size_t)rs * kMsgBytes;
             // chunks 2v and 2v + 1 of this half-row land in one aligned 32-byte sector (the swizzle
             // flips the low bit of the chunk index, or not): one 32-byte store per pair
@@ -805,8 +841,14 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
                 st_global_f32_hint(msg + kPBytes + 4u * h, alpha, keep);
                 if (last) st_global_f32_hint(msg + kPBytes + 4u * (kHeads + h), 1.0f / lrt, keep);
             }
-            // local release; the shipper publishes the slot to the partner
-            mbar_arrive(sm.bar(kBarPStaged + rs));
+            // local release; the shipper publishes the slot to the partner.  An item's last message
+            // goes at once (the partner's epilogue waits for it); the others are released after the
+            // next page's scores have been read, by when their stores are done
+            if (last)
+                mbar_arrive(sm.bar(kBarPStaged + rs));
+            else
+                staged_pending = (int)rs;
+            tr.at(0x37);
         }
         if (hf == 0) {
             const float lse = (m + __log2f(lt)) * 0.69314718055994531f;
@@ -827,13 +869,15 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
 // last pages) goes out at once.  The shipper acquired the rows through the local barriers
 // and the fence is cumulative, so the partner's acquire sees every row.
 __device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, const Sched &sc,
-                                             volatile int *abort) {
+                                             volatile int *abort, Tracer &tr) {
     uint32_t g = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         const uint32_t end = g + (uint32_t)(it.te > it.tb ? it.te - it.tb : 0);
         while (g < end) {
+            tr.at(0x40);
             if (!mbar_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
+            tr.at(0x41);
             uint32_t n = 1;
             while (g + n < end && n < (uint32_t)kMaxBatch &&
                    mbar_test(sm.bar(kBarPStaged + (g + n) % kRing), ((g + n) / kRing) & 1u))
@@ -841,6 +885,7 @@ __device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &
             fence_acq_rel_cluster();
             for (uint32_t k = 0; k < n; ++k)
                 mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPReady + (g + k) % kRing), 1));
+            tr.at(0x4200 + n);
             g += n;
         }
     }
@@ -866,16 +911,19 @@ __device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem 
 // Accumulate CTA, P loader (one thread): ring slot -> shared P buffer, as soon as the
 // partner has published it and the buffer's previous message has been used.
 __device__ __forceinline__ void p_loader_loop(const DecodeParams &p, const Smem &sm, const Sched &sc,
-                                              volatile int *abort, uint32_t &g) {
+                                              volatile int *abort, uint32_t &g, Tracer &tr) {
     const uint8_t *ring = p.ring + (size_t)sc.cid * kRing * kMsgBytes;
     const uint64_t keep = l2_policy_evict_last();
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             const uint32_t rs = g % kRing, jp = g % kPBufs;
+            tr.at(0x60);
             if (!mbar_wait<true>(sm.bar(kBarPReady + rs), (g / kRing) & 1u, abort)) return;
+            tr.at(0x61);
             fence_proxy_async_global();  // the partner's writes, before our async-proxy reads
             if (!mbar_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
+            tr.at(0x62);
             mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
             // P and its factors are contiguous in both places: one copy (the copy engine's cost
             // per transfer is high)
@@ -885,9 +933,9 @@ __device__ __forceinline__ void p_loader_loop(const DecodeParams &p, const Smem 
 }
 // the copies issued last may still be in flight after an abort: wait for them (bounded)
 __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem &sm, const Sched &sc,
-                                              volatile int *abort) {
+                                              volatile int *abort, Tracer &tr) {
     uint32_t g = 0;
-    p_loader_loop(p, sm, sc, abort, g);
+    p_loader_loop(p, sm, sc, abort, g, tr);
     for (uint32_t k = (g > (uint32_t)kPBufs ? g - kPBufs : 0); k < g; ++k)
         if (!mbar_wait_drain(sm.bar(kBarPFull + k % kPBufs), (k / kPBufs) & 1u)) break;
 }
@@ -897,7 +945,7 @@ __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem 
 // the event data is written, then the event barrier gets two arrivals -- this warp's
 // (release: the data is visible) and the MMA commit (all earlier MMAs have completed).
 __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
-                                               volatile int *abort) {
+                                               volatile int *abort, Tracer &tr) {
     const int lane = threadIdx.x & 31;
     uint32_t g = 0, cv = 0;
     bool pending_epilogue = false;
@@ -909,7 +957,9 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
             const uint32_t jp = g % kPBufs;
             const bool first = tile == it.tb, last = tile == it.te - 1;
             const uint32_t valid = (uint32_t)min(kPage, it.n_vis - tile * kPage);
+            tr.at(0x70);
             if (!warp_wait(sm.bar(kBarPFull + jp), (g / kPBufs) & 1u, abort)) return;
+            tr.at(0x71);
             const uint32_t mt = sm.meta(jp);
             if (first) {
                 if (pending_epilogue) {  // the previous item's O must have been read out
@@ -937,13 +987,16 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
                         mma_commit(sm.bar(kBarMmaEvt));
                     }
                     __syncwarp();
+                    tr.at(0x72);
                     if (!warp_wait(sm.bar(kBarCorrEvt), cv & 1u, abort)) return;
+                    tr.at(0x73);
                     ++cv;
                 }
             }
             const uint64_t a0 = sdesc_sw128(sm.pbuf(jp), 16u, 1024u);
             const uint32_t s = g % kStagesV;
             if (!warp_wait(sm.bar(kBarFull + s), (g / kStagesV) & 1u, abort)) return;
+            tr.at(0x74);
             const uint32_t vb = sm.stage(s, kStageV);
             if (last && valid < (uint32_t)kPage) {
                 // rows past the end of the sequence may hold anything (even NaN): zero them,
@@ -974,6 +1027,7 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
                 // an item's last P buffer is released after the epilogue has used it
                 if (!last) mma_commit(sm.bar(kBarPBufFree + jp));
             }
+            tr.at(0x75);
             __syncwarp();
             if (last) {
                 // epilogue event: 1/l per head to the event buffer
@@ -999,8 +1053,8 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
 }
 // every MMA this warp issued has completed before the CTA can free its tensor memory
 __device__ __forceinline__ void role_accum_mma(const DecodeParams &p, const Smem &sm, uint32_t tmem, const Sched &sc,
-                                               volatile int *abort) {
-    accum_mma_loop(p, sm, tmem, sc, abort);
+                                               volatile int *abort, Tracer &tr) {
+    accum_mma_loop(p, sm, tmem, sc, abort, tr);
     if ((threadIdx.x & 31) == 0) {
         mma_commit(sm.bar(kBarDrain));
         mbar_wait_drain(sm.bar(kBarDrain), 0);
@@ -1039,7 +1093,7 @@ __device__ __forceinline__ void stage_and_store(uint32_t stg, int lane, const ui
 }
 
 __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const Smem &sm, uint32_t tmem,
-                                                    const Sched &sc, volatile int *abort) {
+                                                    const Sched &sc, volatile int *abort, Tracer &tr) {
     const int w = threadIdx.x >> 5, q4 = w & 3, hf = w >> 2, lane = threadIdx.x & 31;
     const int h = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -1054,7 +1108,9 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
             continue;
         }
         for (;;) {
+            tr.at(0x80);
             MLA_WAIT_WARP(sm.bar(kBarMmaEvt), ev & 1u, abort);
+            tr.at(0x81);
             ++ev;
             tc_fence_after();
             uint32_t type;
@@ -1076,6 +1132,7 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
                 }
                 tc_fence_before();
                 mbar_arrive(sm.bar(kBarCorrEvt));
+                tr.at(0x82);
                 continue;
             }
             float inv_l;
@@ -1118,6 +1175,7 @@ __device__ __forceinline__ void role_accum_epilogue(const DecodeParams &p, const
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarCorrEvt));
+            tr.at(0x84);
             break;
         }
     }
@@ -1132,6 +1190,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
               const __grid_constant__ CUtensorMap tmap_qc, const __grid_constant__ CUtensorMap tmap_qr,
               const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Tracer tr;
+    tr.at(0x8001);
+    tr.at(0x01);
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
     sm.base = (raw + 1023u) & ~1023u;
@@ -1189,6 +1250,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     // launched as a programmatic dependent of the plan kernel: everything above overlapped it;
     // the plan's results are read only after it has completed
     grid_dependency_wait();
+    tr.at(0x02);
     grid_launch_dependents();  // let the combine kernel's blocks get resident early
     Sched sc;
     sc.cid = (int)cluster_id_x();
@@ -1199,28 +1261,29 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp < 8) {
         if (rank == 0)
-            role_softmax(p, sm, tmem, sc, abort);
+            role_softmax(p, sm, tmem, sc, abort, tr);
         else
-            role_accum_epilogue(p, sm, tmem, sc, abort);
+            role_accum_epilogue(p, sm, tmem, sc, abort, tr);
     } else if (warp == kWarpProducer) {
         if (rank == 0)
-            role_score_producer(p, &tmap_s, &tmap_qc, &tmap_qr, sm, sc, abort);
+            role_score_producer(p, &tmap_s, &tmap_qc, &tmap_qr, sm, sc, abort, tr);
         else
-            role_value_producer(p, &tmap_v, sm, sc, abort);
+            role_value_producer(p, &tmap_v, sm, sc, abort, tr);
     } else if (warp < kWarpMma + 3) {
         if (rank == 0) {
-            if (warp == kWarpMma) role_score_mma<0>(p, sm, tmem, sc, abort);
-            if (warp == kWarpMma + 1) role_score_mma<1>(p, sm, tmem, sc, abort);
+            if (warp == kWarpMma) role_score_mma<0>(p, sm, tmem, sc, abort, tr);
+            if (warp == kWarpMma + 1) role_score_mma<1>(p, sm, tmem, sc, abort, tr);
         } else if (warp == kWarpMma) {
-            role_accum_mma(p, sm, tmem, sc, abort);
+            role_accum_mma(p, sm, tmem, sc, abort, tr);
         } else if (warp == kWarpMma + 1) {
-            if (lane0) role_p_loader(p, sm, sc, abort);
+            if (lane0) role_p_loader(p, sm, sc, abort, tr);
         } else {
             if (lane0) role_releaser(p, sm, sc, abort);
         }
     } else if (warp == kWarpShipper) {
-        if (rank == 0 && lane0) role_shipper(p, sm, sc, abort);
+        if (rank == 0 && lane0) role_shipper(p, sm, sc, abort, tr);
     }
+    tr.at(0x03);
 
     // every thread's own tensor-memory loads and stores have completed (they may be in flight
     // when a role left early after an abort)
@@ -1233,6 +1296,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    tr.at(0x04);
+    tr.at(0x8004);
 }
 
 // ---------------------------------------------------------------------------

@@ -460,6 +460,11 @@ mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream) {
     return launch_error();
 }
 
+#ifdef MLA_TRACE
+// Timeline build only: where the kernels write their per-warp event records (see Tracer).
+int mla_trace_set(void *buf) { return cudaMemcpyToSymbol(g_trace, &buf, sizeof(buf)) == cudaSuccess ? 0 : 6; }
+#endif
+
 mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t *err_word) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
     uint32_t v = 0, z = 0;

@@ -1,6 +1,6 @@
 // ptx.cuh - thin inline-PTX wrappers for the sm_103a primitives the kernels use:
-// mbarriers (with bounded waits), TMA tiled loads, shared->cluster bulk copies,
-// cluster addressing, and the tcgen05 tensor-core / tensor-memory instructions.
+// mbarriers (with bounded waits), TMA tiled loads, cluster addressing, programmatic
+// dependent launch, and the tcgen05 tensor-core / tensor-memory instructions.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -23,6 +23,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// Per-warp event trace, compiled in only with -DMLA_TRACE (a separate build for timeline
+// studies; the library itself is built without it and every call below is empty).  Each warp
+// of each CTA owns kTraceSlots 8-byte records: the event tag in the top 16 bits and the SM's
+// cycle counter (or the global nanosecond timer, for tags >= 0x8000) in the low 48.
+#ifdef MLA_TRACE
+constexpr int kTraceSlots = 2048;
+constexpr int kTraceWarps = 16;
+__device__ uint64_t *g_trace = nullptr;
+struct Tracer {
+    uint64_t *p;
+    uint32_t n;
+    __device__ __forceinline__ Tracer() : n(0) {
+        uint64_t *b = g_trace;
+        p = b ? b + ((size_t)blockIdx.x * kTraceWarps + (threadIdx.x >> 5)) * kTraceSlots : nullptr;
+    }
+    __device__ __forceinline__ void at(uint32_t tag) {
+        if (p != nullptr && (threadIdx.x & 31) == 0 && n < (uint32_t)kTraceSlots) {
+            const uint64_t t = tag >= 0x8000u ? globaltimer_ns() : (uint64_t)clock64();
+            p[n] = ((uint64_t)tag << 48) | (t & 0xFFFFFFFFFFFFull);
+        }
+        ++n;
+    }
+};
+#else
+struct Tracer {
+    __device__ __forceinline__ void at(uint32_t) {}
+};
+#endif
 
 // ----------------------------------------------------------------------------
 // Cluster
@@ -306,5 +335,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// three-input maximum (one instruction on sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// packed pairs of f32 (one 64-bit register pair) and the paired arithmetic on them
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 }  // namespace mla

@@ -3,7 +3,8 @@
 Roles, as in the kernel, for one CTA pair walking its pages g = 0, 1, ... (item boundaries
 included):
 - softmax (score CTA): per page, wait until ring slot g % R is free (PFree), write the message,
-  then mark it staged (PStaged);
+  then mark it staged (PStaged) -- at once on an item's last page, otherwise after the next
+  page's scores have been read (the release then no longer waits for the message's stores);
 - shipper (score CTA): wait for the oldest unpublished message, take the later staged ones of
   the same item (non-blocking tests, at most kMaxBatch), and publish each (PReady on the
   partner);
@@ -43,7 +44,7 @@ class Barrier:
             self.pending = self.count
 
 
-def simulate(items, seed, ring=16, pbufs=4, max_steps=3_000_000, epilogue_release=True):
+def simulate(items, seed, ring=16, pbufs=4, max_steps=3_000_000, epilogue_release=True, deferred=True):
     rnd = random.Random(seed)
     bars = {}
     for j in range(ring):
@@ -81,12 +82,20 @@ def simulate(items, seed, ring=16, pbufs=4, max_steps=3_000_000, epilogue_releas
         return c > k and (c & 1) != (k & 1)
 
     def softmax():
+        pending = None
         for g in range(n_pages):
+            yield  # the page's scores are read
+            if pending is not None:  # the previous message's deferred release
+                bars[f"pstaged{pending}"].arrive()
+                pending = None
             if g >= ring:
                 while not ready(f"pfree{g % ring}", g // ring - 1):
                     yield
             yield  # the message's stores
-            bars[f"pstaged{g % ring}"].arrive()
+            if g in last_of or not deferred:  # an item's last message goes at once
+                bars[f"pstaged{g % ring}"].arrive()
+            else:
+                pending = g % ring
 
     def shipper():
         g = 0
@@ -173,11 +182,11 @@ def random_items(rnd):
     return [rnd.choice([1, 1, 2, 3, 4, 7, 17, 40]) for _ in range(rnd.randint(1, 8))]
 
 
-@pytest.mark.parametrize("ring,pbufs", [(16, 4), (8, 3), (4, 2)])
-def test_ring_protocol_never_aliases(ring, pbufs):
+@pytest.mark.parametrize("ring,pbufs,deferred", [(16, 4, True), (8, 3, True), (4, 2, True), (16, 4, False)])
+def test_ring_protocol_never_aliases(ring, pbufs, deferred):
     for t in range(100):
         rnd = random.Random(9100 + t)
-        simulate(random_items(rnd), seed=t, ring=ring, pbufs=pbufs)
+        simulate(random_items(rnd), seed=t, ring=ring, pbufs=pbufs, deferred=deferred)
 
 
 def test_dropping_the_epilogue_release_is_caught():

@@ -14,7 +14,7 @@ import torch
 
 import mla_latent_kv_77_b300 as mla
 from mla_latent_kv_77_b300 import workloads
-from helpers import check_lse, check_out
+from helpers import check_lse, check_out, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -45,8 +45,16 @@ def test_static_scratch_matches_workspace_entry_point_two_calls_in_a_row():
         assert _static_call(q, pool, bt, sl, case, c["splits"], o, l) == mla.Status.OK
         torch.cuda.synchronize()
         assert mla.get_device_status() == (0, 0)
+        # same plan, same inputs, deterministic kernels: the results must be bit-identical, so
+        # that leftovers of the previous call in the shared array cannot hide under a tolerance
+        assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(l.view(torch.int32), ref_l.view(torch.int32))
         check_out(o, ref_o.double().cpu().numpy(), "o_lat (static scratch)")
         check_lse(l, ref_l.double().cpu().numpy())
+        # and against the fp64 oracle directly
+        or_o, or_l = oracle_decode(case)
+        check_out(o, or_o, "o_lat (static scratch) vs oracle")
+        check_lse(l, or_l)
 
 
 def test_static_scratch_refuses_requests_larger_than_the_array():
@@ -55,8 +63,8 @@ def test_static_scratch_refuses_requests_larger_than_the_array():
     bt, sl = case.block_table.cuda(), case.seq_lens.cuda()
     o = torch.empty(case.B, 1, 128, 512, dtype=torch.bfloat16, device="cuda")
     l = torch.empty(case.B, 1, 128, dtype=torch.float32, device="cuda")
-    # the smallest batch whose workspace exceeds the array (144 queries with the automatic
-    # plan) is refused before anything runs
+    # the smallest batch whose workspace exceeds the array (91 queries with the automatic
+    # plan; 90 is the largest admitted) is refused before anything runs
     limit = 64 << 20  # MLA_STATIC_SCRATCH_BYTES
     n_big = 1
     while mla.decode_workspace_size(n_big, 1, 0) <= limit:
