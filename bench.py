@@ -30,6 +30,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=64 H=128 L=4K"
 UNIT = "tokens/s"
+# the same metric, named for each workload the bench can run (the default one is the first)
+METRICS = {
+    "b64_l4096": METRIC,
+    "b1_l512": "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=1 H=128 L=512",
+    "b128_ragged32k": "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=128 H=128 L~U[1,32K]",
+    "b8_l128k_peaked": "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=8 H=128 L=128K peaked",
+    "b32_tq4_causal_fused": "MLA decode tokens/s and % roofline (HBM GB/s, TC util), B=32 Tq=4 H=128 L=8K causal",
+}
 ROW_BYTES = 576 * 2
 FLOP_PER_TOKEN_QUERY = 2 * 128 * (576 + 512)
 L2_BYTES = 126 * 1024 * 1024
@@ -107,8 +115,8 @@ class _Nvml:
 class ClockSampler:
     """SM clock and throttle reasons sampled during the timed region (read only).
 
-    NVML is polled from a background thread about every millisecond, so even a timed region
-    of a few milliseconds holds samples; only those between mark_begin() and mark_end() are
+    NVML is polled from a background thread about every 0.2 ms, so even a timed region of a
+    couple of milliseconds holds about ten samples; only those between mark_begin() and mark_end() are
     reported.  Without NVML it falls back to nvidia-smi at 100 ms (whose samples then mostly
     fall outside a short timed region; `source` says which was used)."""
 
@@ -119,7 +127,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_s: float = 0.001):
+    def __init__(self, gpu_index: int, period_s: float = 0.0002):
         self.gpu, self.period = gpu_index, period_s
         self.nv = self.proc = None
         self.samples, self.t_begin, self.t_end = [], None, None
@@ -190,7 +198,7 @@ class ClockSampler:
                         reasons.add(name)
             sm = [x[1] for x in win]
             return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.smax,
-                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, about 1 ms, timed region only"}
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, about 0.2 ms, timed region only"}
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         sm, smax, reasons = [], None, set()
@@ -295,7 +303,7 @@ def run_reference(args):
     toks = n * case.Tq
     value = toks * len(times) / sum(times)
     sample = f"{n} of {full_B} sequences x {case.Tq} query tokens x 128 heads per step"
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRICS[args.workload], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "batch": full_B, "q_len": case.Tq, "heads": 128,
@@ -364,6 +372,7 @@ def main():
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        n0 = mla.launch_count()
         clk.mark_begin()
         t_start.record(stream)
         for i in range(args.steps):
@@ -371,6 +380,7 @@ def main():
         t_end.record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
+        launches = mla.launch_count() - n0
     if world > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
@@ -396,31 +406,54 @@ def main():
     t_roof = max(cache_bytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
     mem_bound = cache_bytes / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_tflops"] * 1e12)
 
-    # end to end through the C ABI with host buffers: queries in, latent output + lse out
+    # end to end through the C ABI with host buffers, as a serving loop runs it: every step
+    # uploads its queries from pinned host memory and downloads its latent output and lse.  The
+    # copies run on two copy streams with two device slots, so step i's upload overlaps step
+    # i - 1's decode and step i's download overlaps step i + 1's decode; every copy stays inside
+    # the timed region.
     q_host = q_abs.cpu().pin_memory()
-    o_host = torch.empty(o_lat.shape, dtype=o_lat.dtype).pin_memory()
-    l_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_dev = torch.empty_like(q_abs)
+    o_host = [torch.empty(o_lat.shape, dtype=o_lat.dtype).pin_memory() for _ in range(2)]
+    l_host = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+    q_dev = [torch.empty_like(q_abs) for _ in range(2)]
+    o_dev = [torch.empty_like(o_lat) for _ in range(2)]
+    l_dev = [torch.empty_like(lse) for _ in range(2)]
     h2d = q_host.numel() * q_host.element_size()
-    d2h = o_host.numel() * o_host.element_size() + l_host.numel() * l_host.element_size()
+    d2h = o_host[0].numel() * o_host[0].element_size() + l_host[0].numel() * l_host[0].element_size()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in range(2)]    # slot's queries uploaded
+    ev_dec = [torch.cuda.Event() for _ in range(2)]   # slot's decode done (its queries are free)
+    ev_down = [torch.cuda.Event() for _ in range(2)]  # slot's results downloaded (its outputs are free)
 
-    def e2e_step(i):
-        q_dev.copy_(q_host, non_blocking=True)
-        mla.decode(q_dev, pools[i & 1], bt, sl, case.scale, causal=case.causal, o_lat=o_lat, lse=lse,
+    def e2e_step(i, start):
+        k = i & 1
+        up.wait_event(ev_dec[k] if i >= 2 else start)
+        with torch.cuda.stream(up):
+            q_dev[k].copy_(q_host, non_blocking=True)
+        ev_up[k].record(up)
+        stream.wait_event(ev_up[k])
+        if i >= 2:
+            stream.wait_event(ev_down[k])
+        mla.decode(q_dev[k], pools[i & 1], bt, sl, case.scale, causal=case.causal, o_lat=o_dev[k], lse=l_dev[k],
                    workspace=ws, stream=stream)
-        o_host.copy_(o_lat, non_blocking=True)
-        l_host.copy_(lse, non_blocking=True)
+        ev_dec[k].record(stream)
+        down.wait_event(ev_dec[k])
+        with torch.cuda.stream(down):
+            o_host[k].copy_(o_dev[k], non_blocking=True)
+            l_host[k].copy_(l_dev[k], non_blocking=True)
+        ev_down[k].record(down)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    for rep in range(2):  # the first pass warms up
+        n = args.warmup if rep == 0 else args.steps
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            e2e_step(i, e0)
+        for k in range(min(2, n)):
+            stream.wait_event(ev_down[k])
+        e1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = job_rate(tokens_per_step, args.steps, world, e2e_ms)
 
@@ -434,7 +467,7 @@ def main():
     if rank == 0:
         traffic = profiled_traffic(args.workload)
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": METRICS[args.workload], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "batch": B, "q_len": Tq, "heads": 128, "d_c": 512, "d_r": 64,
@@ -454,7 +487,7 @@ def main():
                          "timed_unit": "one mla_decode call (plan + decode + combine kernels); K calls "
                                        "back to back between one CUDA event pair"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }

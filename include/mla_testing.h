@@ -23,6 +23,15 @@ extern "C" {
  */
 mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream);
 
+/*
+ * mla_test_launch_count - number of kernels the library has enqueued in this
+ * process so far, on any device and stream (every successful launch of every
+ * entry point counts one; host-side argument errors launch and count nothing).
+ * Host only, thread-safe.  Lets a benchmark count the kernels of a timed region
+ * (read it before and after) rather than assume them.
+ */
+uint64_t mla_test_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -69,6 +69,7 @@ EXPORTS = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_version": (_I, []),
     "mla_test_bounded_wait": (_I, [_I, _VP]),
+    "mla_test_launch_count": (ctypes.c_uint64, []),
 }
 
 
@@ -227,6 +228,11 @@ def get_device_status(stream=None) -> Tuple[int, int]:
     w = ctypes.c_uint32(0)
     st = lib().mla_get_device_status(_stream(stream), ctypes.byref(w))
     return int(st), int(w.value)
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().mla_test_launch_count())
 
 
 def test_bounded_wait(limit_ms: int = 50, stream=None) -> None:

@@ -123,7 +123,8 @@ struct PlanHeader {
     int n_bt;
     int max_items;
     int max_slots;
-    int pad[60];
+    int n_split;  // queries split into more than one item (0: the combine kernel has nothing to do)
+    int pad[59];
 };
 // per query (b, t): number of splits, first partial slot, tiles, first item
 struct BtInfo {
@@ -305,9 +306,12 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
         items_local += splits[bt];
         slots_local += splits[k] > 1 ? splits[k] : 0;
     }
-    int n_items, n_slots;
+    int n_items, n_slots, n_split;
     int ioff = block_excl_scan(items_local, s_tmp, &n_items);
     int soff = block_excl_scan(slots_local, s_tmp, &n_slots);
+    int split_local = 0;
+    for (int k = tid * per; k < min(n_bt, (tid + 1) * per); ++k) split_local += splits[k] > 1 ? 1 : 0;
+    block_excl_scan(split_local, s_tmp, &n_split);
     const bool overflow = n_items > max_items || n_slots > max_slots;
     for (int k = tid * per; k < min(n_bt, (tid + 1) * per); ++k) {
         int bt = sorted ? s_ord[k] : k;
@@ -347,6 +351,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int
     if (tid == 0) {
         if (overflow) raise_status(0x8u);
         hdr->n_items = overflow ? 0 : n_items;
+        hdr->n_split = overflow ? 0 : n_split;
         hdr->n_bt = n_bt;
         hdr->max_items = max_items;
         hdr->max_slots = max_slots;
@@ -1339,19 +1344,25 @@ __device__ __forceinline__ void combine_row(const float *o_base, size_t o_stride
     if (write_lse) *lse_out = L;
 }
 
-// grid (n_bt, 16), block 128: queries that were split into more than one item
+// block 128, one wave of blocks: each takes (query, 8-head group) units in turn and merges the
+// queries that were split into more than one item.  When the plan split nothing, every block
+// returns after one read of the plan header.
 __global__ void __launch_bounds__(128)
-combine_kernel(const BtInfo *__restrict__ info, const float *__restrict__ part_o,
+combine_kernel(const PlanHeader *__restrict__ hdr, const BtInfo *__restrict__ info, const float *__restrict__ part_o,
                const float *__restrict__ part_lse, __nv_bfloat16 *__restrict__ o_lat, float *__restrict__ lse) {
     grid_dependency_wait();  // launched as a programmatic dependent of the decode kernel
-    const int bt = blockIdx.x;
-    const BtInfo in = info[bt];
-    if (in.splits <= 1) return;
-    const int h = blockIdx.y * 8 + (threadIdx.x >> 4);
-    const int col0 = (threadIdx.x & 15) * 32;
-    combine_row(part_o + ((size_t)in.slot_base * kHeads + h) * kDc, (size_t)kHeads * kDc,
-                part_lse + (size_t)in.slot_base * kHeads + h, kHeads, in.splits, col0,
-                o_lat + ((size_t)bt * kHeads + h) * kDc, lse + (size_t)bt * kHeads + h, (threadIdx.x & 15) == 0);
+    if (hdr->n_split == 0) return;
+    const int n_units = hdr->n_bt * (kHeads / 8);
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int bt = u / (kHeads / 8);
+        const BtInfo in = info[bt];
+        if (in.splits <= 1) continue;
+        const int h = (u % (kHeads / 8)) * 8 + (threadIdx.x >> 4);
+        const int col0 = (threadIdx.x & 15) * 32;
+        combine_row(part_o + ((size_t)in.slot_base * kHeads + h) * kDc, (size_t)kHeads * kDc,
+                    part_lse + (size_t)in.slot_base * kHeads + h, kHeads, in.splits, col0,
+                    o_lat + ((size_t)bt * kHeads + h) * kDc, lse + (size_t)bt * kHeads + h, (threadIdx.x & 15) == 0);
+    }
 }
 
 // grid ceil(rows / 8), block 128: dense parts [n_parts, rows, 512]

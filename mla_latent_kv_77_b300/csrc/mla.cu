@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -208,8 +209,13 @@ __global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
     }
 }
 
-mla_status_t launch_error() {
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+// kernels enqueued so far (see mla_test_launch_count)
+std::atomic<uint64_t> g_launches{0};
+
+mla_status_t launch_error(uint64_t kernels = 1) {
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    g_launches += kernels;
+    return MLA_OK;
 }
 
 // Device address of the library-owned decode scratch on each device, looked up once.
@@ -392,16 +398,18 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
         return MLA_ERR_CUDA;
     }
     cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3(n_bt, kHeads / 8, 1);
+    const int units = n_bt * (kHeads / 8);
+    ccfg.gridDim = dim3(units < 2 * info->sms ? units : 2 * info->sms, 1, 1);
     ccfg.blockDim = dim3(128, 1, 1);
     ccfg.stream = s;
     ccfg.attrs = &at[1];
     ccfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&ccfg, combine_kernel, (const BtInfo *)bt_info, (const float *)p.part_o,
+    if (cudaLaunchKernelEx(&ccfg, combine_kernel, (const PlanHeader *)hdr, (const BtInfo *)bt_info, (const float *)p.part_o,
                            (const float *)p.part_lse, p.o_lat, lse) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
+    g_launches += 3;  // plan, decode, combine
     return MLA_OK;
 }
 
@@ -464,6 +472,8 @@ mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream) {
 // Timeline build only: where the kernels write their per-warp event records (see Tracer).
 int mla_trace_set(void *buf) { return cudaMemcpyToSymbol(g_trace, &buf, sizeof(buf)) == cudaSuccess ? 0 : 6; }
 #endif
+
+uint64_t mla_test_launch_count(void) { return g_launches.load(); }
 
 mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t *err_word) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
