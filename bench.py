@@ -271,6 +271,58 @@ def cpu_oracle_rate(case, budget_s: float = 12.0, max_seqs: int = None):
     return toks / dt, cores, f"{n} of {B} sequences x {case.Tq} query tokens x 128 heads ({dt:.1f} s)"
 
 
+def fused_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
+    """The fused absorb -> decode -> up-projection chain on the batch-32, 4-query causal
+    workload (8192 + 4 cached tokens per sequence): each call's device time, K calls back to
+    back between one event pair, and its fraction of the HBM roofline over its algorithmic bytes
+    (weights, inputs and outputs for the two GEMMs; the cache rows for the decode)."""
+    import torch
+    case = workloads.make_workload("b32_tq4_causal_fused", seed=0, device=dev)
+    B, Tq = case.B, case.Tq
+    n = B * Tq
+    qn, qr = case.q_nope.reshape(n, 128, 128), case.q_rope.reshape(n, 128, 64)
+    q_abs = torch.empty(n, 128, 576, dtype=torch.bfloat16, device=dev)
+    o_lat = torch.empty(B, Tq, 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Tq, 128, dtype=torch.float32, device=dev)
+    out = torch.empty(n, 128, 128, dtype=torch.bfloat16, device=dev)
+    bt, sl = case.block_table.to(dev), case.seq_lens.to(dev)
+    ws = torch.empty(mla.decode_workspace_size(B, Tq, 0), dtype=torch.uint8, device=dev)
+    calls = {
+        "mla_absorb_q": lambda: mla.absorb_q(qn, qr, case.w_uk, out=q_abs, stream=stream),
+        "mla_decode": lambda: mla.decode(q_abs.view(B, Tq, 128, 576), case.pool, bt, sl, case.scale, causal=True,
+                                         o_lat=o_lat, lse=lse, workspace=ws, stream=stream),
+        "mla_up_proj": lambda: mla.up_proj(o_lat.view(n, 128, 512), case.w_uv, out=out, stream=stream),
+    }
+    w_bytes = 128 * 128 * 512 * 2
+    bytes_ = {
+        "mla_absorb_q": w_bytes + n * 128 * (128 + 64) * 2 + n * 128 * 576 * 2,
+        "mla_decode": int(case.seq_lens.to(torch.int64).sum()) * ROW_BYTES,
+        "mla_up_proj": w_bytes + n * 128 * 512 * 2 + n * 128 * 128 * 2,
+    }
+    res = {"workload": "b32_tq4_causal_fused", "tokens": n, "unit": "us per call"}
+    for name, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / steps
+        gbs = bytes_[name] / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "bytes": bytes_[name], "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
+    flops = 2 * 128 * sum(max(0, 8196 - (Tq - 1 - t)) for t in range(Tq)) * B * (576 + 512)
+    res["mla_decode"]["tensor_frac"] = flops / (res["mla_decode"]["us"] * 1e-6) / 1e12 / pk["bf16_tflops"]
+    res["chain_us"] = sum(res[k]["us"] for k in calls)
+    st, word = mla.get_device_status()
+    assert st == 0, f"device status {word:#x}"
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each step
     decodes a bounded sample (`--ref-seqs` whole sequences, all heads and query tokens) of
@@ -322,6 +374,7 @@ def main():
     ap.add_argument("--workload", default="b64_l4096")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused absorb/decode/up-projection timing")
     ap.add_argument("--ref-seqs", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -457,6 +510,10 @@ def main():
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = job_rate(tokens_per_step, args.steps, world, e2e_ms)
 
+    fused = None
+    if rank == 0 and args.workload == "b64_l4096" and not args.no_fused:
+        fused = fused_leg(mla, workloads, dev, stream, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks())
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if case.q_abs is None:
@@ -490,6 +547,7 @@ def main():
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
+            "fused": fused,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -55,13 +55,14 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
             // every kernel of a decode call asks for the maximum shared-memory carveout, so the
             // SMs need not switch their L1 / shared split between the plan, decode and combine
             for (const void *fn : {(const void *)plan_kernel, (const void *)combine_kernel,
-                                   (const void *)combine_rows_kernel, (const void *)decode_kernel})
+                                   (const void *)combine_rows_kernel, (const void *)decode_kernel,
+                                   (const void *)head_gemm_kernel})
                 cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
             cudaGetLastError();
             if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmem) !=
                     cudaSuccess ||
-                cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
+                cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemMax) !=
                     cudaSuccess)
                 return MLA_ERR_CUDA;
             cudaLaunchConfig_t cfg = {};
@@ -120,6 +121,21 @@ bool tmap_row_blocks(CUtensorMap *m, const void *base, uint64_t rows, uint32_t b
     cuuint64_t dims[3] = {64, rows, (cuuint64_t)kBoxesS};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 128};
     cuuint32_t box[3] = {64, box_rows, blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D view (64 columns, rows, blocks) of a [rows, 64 * blocks] bf16 array with strides (2 B,
+// row bytes, 128 B): a box of (64, box_rows, box_blocks) lands as `box_blocks` consecutive
+// box_rows x 128-byte swizzled blocks (the row-block view of mla_decode's pages, for any width)
+bool tmap_col_blocks(CUtensorMap *m, const void *base, uint64_t rows, uint32_t blocks, uint32_t box_rows,
+                     uint32_t box_blocks) {
+    cuuint64_t dims[3] = {64, rows, blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)blocks * 128, 128};
+    cuuint32_t box[3] = {64, box_rows, box_blocks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -262,6 +278,19 @@ size_t mla_decode_workspace_size(int batch, int q_len, int num_splits) {
     return w.total;
 }
 
+// 3-D bf16 view (cols, heads, tokens) of a [tokens, 128, cols] output for the GEMMs' TMA stores:
+// boxes of 128 columns x 1 head x 128 tokens, no swizzle (the staged tile is plain row-major)
+bool tmap_out(CUtensorMap *m, const void *base, uint64_t cols, uint64_t n_tokens) {
+    cuuint64_t dims[3] = {cols, (cuuint64_t)kHeads, n_tokens};
+    cuuint64_t strides[2] = {cols * 2, cols * 2 * kHeads};
+    cuuint32_t box[3] = {128, 1, (cuuint32_t)kGemmTileN};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 mla_status_t mla_absorb_q(const void *q_nope, const void *q_rope, const void *w_uk, void *q_abs, int n_tokens,
                           int n_heads, mla_stream_t stream) {
     if (!q_nope || !q_rope || !w_uk || !q_abs) return MLA_ERR_INVALID_ARG;
@@ -273,17 +302,18 @@ mla_status_t mla_absorb_q(const void *q_nope, const void *q_rope, const void *w_
     DeviceInfo *info;
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
-    CUtensorMap tw, tx;
-    if (!tmap_2d(&tw, w_uk, kDc, (uint64_t)kHeads * 128, kDc * 2, 64, 64)) return MLA_ERR_CUDA;
+    CUtensorMap tw, tx, to;
+    if (!tmap_col_blocks(&tw, w_uk, (uint64_t)kHeads * 128, kDc / 64, 64, kDc / 64)) return MLA_ERR_CUDA;
     if (!tmap_2d(&tx, q_nope, (uint64_t)kHeads * 128, (uint64_t)n_tokens, (uint64_t)kHeads * 128 * 2, 64, 128))
         return MLA_ERR_CUDA;
+    if (!tmap_out(&to, q_abs, kD, (uint64_t)n_tokens)) return MLA_ERR_CUDA;
     GemmParams p;
     p.mode = kModeAbsorb;
     p.n_tokens = n_tokens;
     p.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
-    p.out = static_cast<__nv_bfloat16 *>(q_abs);
-    dim3 grid(kHeads, kDc / 128, (n_tokens + kGemmTileN - 1) / kGemmTileN);
-    head_gemm_kernel<<<grid, 192, kGemmSmem, (cudaStream_t)stream>>>(tw, tx, p);
+    p.q_abs = static_cast<__nv_bfloat16 *>(q_abs);
+    dim3 grid(kHeads, (n_tokens + kGemmTileN - 1) / kGemmTileN);
+    head_gemm_kernel<<<grid, kGemmThreads, gemm_smem(kAbsorbRegion), (cudaStream_t)stream>>>(tw, tx, to, p);
     return launch_error();
 }
 
@@ -298,17 +328,18 @@ mla_status_t mla_up_proj(const void *o_lat, const void *w_uv, void *out, int n_t
     DeviceInfo *info;
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx, to;
     if (!tmap_2d(&tw, w_uv, kDc, (uint64_t)kHeads * 128, kDc * 2, 64, 128)) return MLA_ERR_CUDA;
     if (!tmap_2d(&tx, o_lat, (uint64_t)kHeads * kDc, (uint64_t)n_tokens, (uint64_t)kHeads * kDc * 2, 64, 128))
         return MLA_ERR_CUDA;
+    if (!tmap_out(&to, out, 128, (uint64_t)n_tokens)) return MLA_ERR_CUDA;
     GemmParams p;
     p.mode = kModeUpProj;
     p.n_tokens = n_tokens;
     p.q_rope = nullptr;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    dim3 grid(kHeads, 1, (n_tokens + kGemmTileN - 1) / kGemmTileN);
-    head_gemm_kernel<<<grid, 192, kGemmSmem, (cudaStream_t)stream>>>(tw, tx, p);
+    p.q_abs = nullptr;
+    dim3 grid(kHeads, (n_tokens + kGemmTileN - 1) / kGemmTileN);
+    head_gemm_kernel<<<grid, kGemmThreads, gemm_smem(kUpRegion), (cudaStream_t)stream>>>(tw, tx, to, p);
     return launch_error();
 }
 
