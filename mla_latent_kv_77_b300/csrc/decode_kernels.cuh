@@ -55,7 +55,12 @@ constexpr int kMaxBatch = 4;         // most messages published behind one clust
 constexpr int kPBytes = kHeads * kPage * 2;  // 16 KB of bf16 probabilities
 constexpr int kMetaBytes = 1024;     // alpha[128] f32, inv_l[128] f32
 constexpr uint32_t kMsgBytes = kPBytes + kMetaBytes;  // one message: P, then its factors
-constexpr float kTau = 8.0f;         // lazy rescale threshold, log2 units (factor 256)
+// Lazy rescale threshold, log2 units: the running reference m moves only when a page maximum
+// exceeds it by more than this.  Probabilities are then at most 2^40 relative to m: bf16 P and
+// fp32 row sums and O keep their relative precision at any scale, and with at most 2^17 tokens
+// and |values| far below 2^60 nothing overflows fp32 (2^127).  A small threshold (8) made
+// peaked rows rescale O on about a quarter of the pages of a 128K context.
+constexpr float kTau = 40.0f;
 constexpr int kMaxClusters = 80;     // CTA pairs the workspace is sized for (B300: 74)
 
 // TMEM columns

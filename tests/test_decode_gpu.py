@@ -172,3 +172,41 @@ def test_bounded_wait_gives_up_and_context_survives():
     o, lse = mla.decode(q, pool, bt, sl, case.scale)
     assert mla.get_device_status() == (0, 0)
     check_out(o, oracle_decode(case)[0])
+
+
+@pytest.mark.parametrize("batch,q_len,causal", [(1100, 1, False), (700, 3, True)])
+def test_large_batches_of_short_sequences(batch, q_len, causal):
+    """Batches whose query count passes the planner's one-query-per-thread limit (1024: the
+    queries are no longer sorted) and its shared-memory limit (2048: the planner's arrays move to
+    the workspace), with short ragged sequences over a shuffled pool, against the oracle on every
+    query."""
+    g = torch.Generator().manual_seed(41 + batch)
+    lens = [int(x) for x in torch.randint(1, 160, (batch,), generator=g)]
+    if causal:
+        lens = [max(L, q_len) for L in lens]
+    case = workloads.make_case("many", lens, Tq=q_len, causal=causal, shuffle=True, spare_pages=7,
+                               garbage="nan", seed=43)
+    assert case.B * case.Tq > (2048 if q_len > 1 else 1024)
+    _clear_status()
+    q, pool, bt, sl = _gpu(case)
+    o, lse = mla.decode(q, pool, bt, sl, case.scale, causal=causal)
+    assert mla.get_device_status() == (0, 0)
+    ref_o, ref_lse = oracle_decode(case)
+    check_out(o, ref_o)
+    check_lse(lse, ref_lse)
+
+
+def test_b1_l512_fused_chain_matches_naive_oracle():
+    """The single-sequence, 512-token workload at its own shape (contiguous cache as 8 identity
+    pages) through absorb -> decode -> up-projection, against the naive form that rebuilds every
+    head's keys and values (explainer Steps 5-7)."""
+    case = workloads.make_workload("b1_l512", seed=0)
+    qn, qr, wk, wv = (t.to(DEV) for t in (case.q_nope, case.q_rope, case.w_uk, case.w_uv))
+    q_abs = mla.absorb_q(qn, qr, wk)
+    o, lse = mla.decode(q_abs, case.pool.to(DEV), case.block_table.to(DEV), case.seq_lens.to(DEV), case.scale)
+    out = mla.up_proj(o, wv)
+    assert mla.get_device_status() == (0, 0)
+    ref_out, ref_lse = oracle.decode_naive(case.q_nope, case.q_rope, case.w_uk, case.w_uv, case.pool,
+                                           case.block_table, case.seq_lens, case.scale, causal=False)
+    check_out(out, ref_out, "out")
+    check_lse(lse, ref_lse)
