@@ -10,7 +10,8 @@ to float32 (bf16 values are exact in float32); every result is float64.
 
 Sources (see the C file for the passage each function follows):
   * "DeepSeek-V2" explainer, Steps 5-8 (latent cache, absorption, decoupled
-    RoPE, 576-number cache row);
+    RoPE, 576-number cache row; the cache write c = W^DKV h of equation 9 and
+    the rotated key k^R of Step 7);
   * DeepSeek-V2 paper breakdown, "How It Works" (latent c_t cached, up-projected
     to K and V, separate RoPE key kept beside it).
 """
@@ -30,6 +31,7 @@ _lib = None
 _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
 
 
 def build(force: bool = False) -> str:
@@ -60,8 +62,12 @@ def _load():
                                             ctypes.c_double, ctypes.c_int, ctypes.c_int, _f64p, _f64p]
         lib.oracle_combine.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_long, ctypes.c_int,
                                        _f64p, _f64p]
+        lib.oracle_rope.argtypes = [_f64p, ctypes.c_double, ctypes.c_int, ctypes.c_double, _f64p]
+        lib.oracle_cache_append.argtypes = [_f32p, _f32p, _f32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_double, _f64p, _i64p]
         for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed",
-                   "oracle_decode_naive", "oracle_combine"):
+                   "oracle_decode_naive", "oracle_combine", "oracle_rope", "oracle_cache_append"):
             getattr(lib, fn).restype = None
         _lib = lib
     return _lib
@@ -190,3 +196,35 @@ def combine(o_parts, lse_parts):
     lse = np.zeros(l.shape[1:], dtype=np.float64)
     _load().oracle_combine(o, l, R, M, d, out, lse)
     return out, lse
+
+
+def rope(x, pos: float, base: float = 10000.0) -> np.ndarray:
+    """Rotate the pairs (2i, 2i+1) of x [d] by pos * base^(-2i/d)  (Step 7, decoupled RoPE key)."""
+    v = _f64(x).reshape(-1)
+    out = np.zeros_like(v)
+    _load().oracle_rope(v, float(pos), int(v.size), float(base), out)
+    return out
+
+
+def cache_append(h, w_dkv, w_kr, block_table, seq_lens, q_len: int, num_pages: int, page: int = 64,
+                 rope_base: float = 10000.0):
+    """Cache rows of new tokens and the pool rows they go to (Step 5 eq. 9 and Step 7).
+
+    h [B*Tq, d_model] (or [B, Tq, d_model]), w_dkv [d_c, d_model], w_kr [d_r, d_model],
+    block_table [B, max_pages], seq_lens [B] (already counting the Tq new tokens).
+    Returns (rows [B*Tq, d_c + d_r] float64, slot [B*Tq] int64; -1 for a token with no valid slot).
+    """
+    x = _f32(h)
+    wd, wr = _f32(w_dkv), _f32(w_kr)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    B, max_pages = bt.shape
+    d_c, d_model = wd.shape
+    d_r = wr.shape[0]
+    x = x.reshape(B * q_len, d_model)
+    rows = np.zeros((B * q_len, d_c + d_r), dtype=np.float64)
+    slot = np.zeros(B * q_len, dtype=np.int64)
+    if wr.size == 0:
+        wr = np.zeros(1, dtype=np.float32)
+    _load().oracle_cache_append(x, wd, wr, bt, sl, B, int(q_len), d_model, d_c, d_r, int(page), max_pages,
+                                int(num_pages), float(rope_base), rows, slot)
+    return rows, slot

@@ -349,3 +349,83 @@ void oracle_combine(const double *o_parts, const double *lse_parts, int R, long 
         lse[i] = L;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Cache write for new tokens.                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Rotary position embedding of one vector ("DeepSeek-V2" explainer, Step 7:
+ * order is encoded by turning each query and key through an angle that grows
+ * in proportion to the token's position, so that a query-key score depends
+ * only on their distance).  The pages give no formula; the reading taken:
+ *   - coordinates (2i, 2i+1) form pair i, i = 0 .. d/2 - 1;
+ *   - pair i turns counter-clockwise by pos * theta_i,
+ *     theta_i = base^(-2i/d), base given by the caller (10000 by default);
+ *   - out[2i]   = x[2i] cos(a) - x[2i+1] sin(a)
+ *     out[2i+1] = x[2i] sin(a) + x[2i+1] cos(a),   a = pos * theta_i.
+ * `pos` is a double so that tests can place a vector at any angle.
+ */
+void oracle_rope(const double *x, double pos, int d, double base, double *out) {
+    for (int i = 0; i < d / 2; ++i) {
+        const double theta = pow(base, -2.0 * (double)i / (double)d);
+        const double a = pos * theta;
+        const double c = cos(a), s = sin(a);
+        const double x0 = x[2 * i], x1 = x[2 * i + 1];
+        out[2 * i] = x0 * c - x1 * s;
+        out[2 * i + 1] = x0 * s + x1 * c;
+    }
+}
+
+/*
+ * The cache row of each new token (explainer Step 5, the paper's equation 9:
+ * the hidden vector h is projected down to the latent c = W^DKV h; Step 7:
+ * the token's one shared position key is k^R = RoPE(W^KR h); Step 8: the row
+ * kept per token is [c | k^R], d_c + d_r numbers) and the pool row it is
+ * written to.
+ *   h        [B*Tq, d_model]  the new tokens, sequence-major
+ *   w_dkv    [d_c, d_model]   row-major: c[r] = sum_k w_dkv[r][k] h[k]
+ *   w_kr     [d_r, d_model]   row-major, likewise for the unrotated k^R
+ *   block_table [B, max_pages], seq_lens [B]: the lengths already count the
+ *            Tq new tokens, so token t of sequence b has position
+ *            p = seq_lens[b] - Tq + t, the same convention as the causal
+ *            decode above.
+ * Outputs: rows [B*Tq, d_c + d_r] (the row values, double) and slot [B*Tq],
+ * the pool row block_table[b, p / page] * page + p % page, or -1 where p is
+ * negative or beyond the block table, or the table entry is outside
+ * [0, num_pages).
+ */
+void oracle_cache_append(const float *h, const float *w_dkv, const float *w_kr, const int32_t *block_table,
+                         const int32_t *seq_lens, int B, int Tq, int d_model, int d_c, int d_r, int page,
+                         int max_pages, int num_pages, double rope_base, double *rows, int64_t *slot) {
+    const int D = d_c + d_r;
+    double *kr = (double *)malloc(sizeof(double) * (size_t)(d_r > 0 ? d_r : 1));
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < Tq; ++t) {
+            const long n = (long)b * Tq + t;
+            const float *x = h + (size_t)n * d_model;
+            double *row = rows + (size_t)n * D;
+            /* c = W^DKV h */
+            for (int r = 0; r < d_c; ++r) {
+                double acc = 0.0;
+                for (int k = 0; k < d_model; ++k) acc += (double)w_dkv[(size_t)r * d_model + k] * (double)x[k];
+                row[r] = acc;
+            }
+            /* k^R = RoPE(W^KR h) at the token's position */
+            for (int r = 0; r < d_r; ++r) {
+                double acc = 0.0;
+                for (int k = 0; k < d_model; ++k) acc += (double)w_kr[(size_t)r * d_model + k] * (double)x[k];
+                kr[r] = acc;
+            }
+            const long p = (long)seq_lens[b] - Tq + t;
+            oracle_rope(kr, (double)p, d_r, rope_base, row + d_c);
+            /* where the row goes */
+            slot[n] = -1;
+            if (p >= 0 && p / page < max_pages) {
+                const int32_t pg = block_table[(size_t)b * max_pages + p / page];
+                if (pg >= 0 && pg < num_pages) slot[n] = (int64_t)pg * page + p % page;
+            }
+        }
+    }
+    free(kr);
+}

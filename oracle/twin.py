@@ -1,4 +1,4 @@
-"""Pure-Python brute-force twin of the MLA decode, for tiny shapes only.
+"""Pure-Python brute-force twin of the MLA decode and cache write, for tiny shapes only.
 
 TEST INFRASTRUCTURE ONLY (imported by tests).  Written separately from
 ``mla_oracle.c`` and structured differently on purpose, so that a slip in one
@@ -16,9 +16,14 @@ is unlikely to be repeated in the other:
 It has no paged layout of its own beyond resolving the block table to a row
 list, and no absorbed form: agreement of the C oracle's absorbed form with
 this twin therefore checks the Step 6 associativity independently.
+
+The cache write (Step 5's c = W^DKV h, Step 7's rotated k^R) turns each RoPE
+pair as a complex number times a unit phasor, where the C oracle writes out
+the cosine/sine rotation; and it finds a token's pool row with ``divmod``.
 """
 from __future__ import annotations
 
+import cmath
 import math
 from typing import List, Sequence
 
@@ -98,3 +103,35 @@ def decode(q_nope, q_rope, W_uk, W_uv, pool, block_table, seq_lens, scale, causa
         out.append(ob)
         lse.append(lb)
     return out, lse
+
+
+def rope_phasor(x: Sequence[float], pos: float, base: float) -> List[float]:
+    """Step 7's rotation written with complex numbers: pair i is the complex number
+    x[2i] + 1j * x[2i+1], multiplied by the unit phasor exp(1j * pos * base**(-2i/d))."""
+    d = len(x)
+    out: List[float] = []
+    for i in range(d // 2):
+        z = complex(x[2 * i], x[2 * i + 1]) * cmath.exp(1j * pos * base ** (-(2.0 * i) / d))
+        out += [z.real, z.imag]
+    return out
+
+
+def cache_rows(h, W_dkv, W_kr, block_table, seq_lens, q_len: int, page: int, num_pages: int, base: float):
+    """Brute-force cache write (Step 5 eq. 9 and Step 7), one token at a time over nested lists.
+
+    h[b][t][d_model]; returns {pool row index: row values} for every token that has a valid slot.
+    A token's position is its index in the sequence once the q_len new tokens are counted.
+    """
+    written = {}
+    for b, toks in enumerate(h):
+        first = seq_lens[b] - q_len
+        for t, x in enumerate(toks):
+            pos = first + t
+            logical_page, offset = divmod(pos, page) if pos >= 0 else (-1, 0)
+            if pos < 0 or logical_page >= len(block_table[b]):
+                continue
+            phys = block_table[b][logical_page]
+            if not 0 <= phys < num_pages:
+                continue
+            written[phys * page + offset] = _matvec(W_dkv, x) + rope_phasor(_matvec(W_kr, x), pos, base)
+    return written
