@@ -271,11 +271,45 @@ def cpu_oracle_rate(case, budget_s: float = 12.0, max_seqs: int = None):
     return toks / dt, cores, f"{n} of {B} sequences x {case.Tq} query tokens x 128 heads ({dt:.1f} s)"
 
 
+def graph_us(calls, reps: int) -> float:
+    """Device time per call of `calls` (each takes the stream to enqueue on), captured once into a
+    CUDA graph and replayed `reps` times back to back between one event pair: the host's per-call
+    cost (argument checks, tensor-map encoding, Python) stays out of the timed region, as in a
+    serving loop that replays a captured decode step."""
+    import torch
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        for c in calls:
+            c(gs)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (reps * len(calls))
+    del g
+    return us
+
+
+def _l2_copies(bytes_per_copy: int) -> int:
+    """Copies of a call's inputs that cover twice the 126 MB L2, so no call finds its inputs cached."""
+    return max(2, -(-2 * 126 * 2 ** 20 // bytes_per_copy))
+
+
 def fused_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
     """The fused absorb -> decode -> up-projection chain on the batch-32, 4-query causal
-    workload (8192 + 4 cached tokens per sequence): each call's device time, K calls back to
-    back between one event pair, and its fraction of the HBM roofline over its algorithmic bytes
-    (weights, inputs and outputs for the two GEMMs; the cache rows for the decode)."""
+    workload (8192 + 4 cached tokens per sequence).  Each call and the whole chain are captured
+    into CUDA graphs and replayed (graph_us).  Inputs larger than L2: the GEMMs cycle through
+    copies of their 16.8 MB weights covering twice the L2, and the decode streams 302 MB of cache.
+    Fractions are of the HBM roofline over algorithmic bytes (weights, inputs and outputs for the
+    GEMMs; the cache rows for the decode)."""
     import torch
     case = workloads.make_workload("b32_tq4_causal_fused", seed=0, device=dev)
     B, Tq = case.B, case.Tq
@@ -287,39 +321,95 @@ def fused_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
     out = torch.empty(n, 128, 128, dtype=torch.bfloat16, device=dev)
     bt, sl = case.block_table.to(dev), case.seq_lens.to(dev)
     ws = torch.empty(mla.decode_workspace_size(B, Tq, 0), dtype=torch.uint8, device=dev)
-    calls = {
-        "mla_absorb_q": lambda: mla.absorb_q(qn, qr, case.w_uk, out=q_abs, stream=stream),
-        "mla_decode": lambda: mla.decode(q_abs.view(B, Tq, 128, 576), case.pool, bt, sl, case.scale, causal=True,
-                                         o_lat=o_lat, lse=lse, workspace=ws, stream=stream),
-        "mla_up_proj": lambda: mla.up_proj(o_lat.view(n, 128, 512), case.w_uv, out=out, stream=stream),
-    }
     w_bytes = 128 * 128 * 512 * 2
+    copies = _l2_copies(w_bytes)
+    w_uk = [case.w_uk.clone() for _ in range(copies)]
+    w_uv = [case.w_uv.clone() for _ in range(copies)]
+
+    def absorb(i):
+        return lambda st: mla.absorb_q(qn, qr, w_uk[i % copies], out=q_abs, stream=st)
+
+    def decode(st):
+        mla.decode(q_abs.view(B, Tq, 128, 576), case.pool, bt, sl, case.scale, causal=True, o_lat=o_lat, lse=lse,
+                   workspace=ws, stream=st)
+
+    def up(i):
+        return lambda st: mla.up_proj(o_lat.view(n, 128, 512), w_uv[i % copies], out=out, stream=st)
+    for i in range(warmup):
+        absorb(i)(stream)
+        decode(stream)
+        up(i)(stream)
+    torch.cuda.synchronize()
+    us = {
+        "mla_absorb_q": graph_us([absorb(i) for i in range(copies)], max(1, steps // copies)),
+        "mla_decode": graph_us([decode] * 10, max(1, steps // 10)),
+        "mla_up_proj": graph_us([up(i) for i in range(copies)], max(1, steps // copies)),
+    }
+    chain = []
+    for i in range(8):
+        chain += [absorb(i), decode, up(i)]
+    chain_us = graph_us(chain, max(1, steps // 8)) * 3
     bytes_ = {
         "mla_absorb_q": w_bytes + n * 128 * (128 + 64) * 2 + n * 128 * 576 * 2,
         "mla_decode": int(case.seq_lens.to(torch.int64).sum()) * ROW_BYTES,
         "mla_up_proj": w_bytes + n * 128 * 512 * 2 + n * 128 * 128 * 2,
     }
-    res = {"workload": "b32_tq4_causal_fused", "tokens": n, "unit": "us per call"}
-    for name, fn in calls.items():
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1000.0 / steps
-        gbs = bytes_[name] / (us * 1e-6) / 1e9
-        res[name] = {"us": us, "bytes": bytes_[name], "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
+    res = {"workload": "b32_tq4_causal_fused", "tokens": n, "unit": "us per call", "steps": steps,
+           "timing": "CUDA-graph replays; GEMM weights rotate over %d copies (2 x L2)" % copies}
+    for k in us:
+        gbs = bytes_[k] / (us[k] * 1e-6) / 1e9
+        res[k] = {"us": us[k], "bytes": bytes_[k], "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
     flops = 2 * 128 * sum(max(0, 8196 - (Tq - 1 - t)) for t in range(Tq)) * B * (576 + 512)
     res["mla_decode"]["tensor_frac"] = flops / (res["mla_decode"]["us"] * 1e-6) / 1e12 / pk["bf16_tflops"]
-    res["chain_us"] = sum(res[k]["us"] for k in calls)
+    res["chain_us"] = chain_us
     st, word = mla.get_device_status()
     assert st == 0, f"device status {word:#x}"
-    del case
+    del case, w_uk, w_uv
     torch.cuda.empty_cache()
+    return res
+
+
+def append_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
+    """The cache write (mla_cache_append: c = W^DKV h, rotated k^R, scattered into the pool) on its
+    three workloads: one decode step's 64 new tokens, the causal step's 128, and a 4096-token
+    prompt, all at d_model 5120.  Captured into a CUDA graph and replayed (graph_us); inputs larger
+    than L2: the calls cycle through copies of (h, W^DKV, W^KR) covering twice the 126 MB L2.
+    Roofline: the HBM bytes a call must move (both weights, h, the written rows) and the tensor
+    FLOPs (2 x tokens x 576 x d_model); the prompt is the tensor-bound one."""
+    import torch
+    res = {"unit": "us per call", "steps": steps, "d_model": workloads.D_MODEL,
+           "timing": "CUDA-graph replays; inputs rotate over copies covering 2 x 126 MB of L2"}
+    for name in workloads.APPEND_WORKLOADS:
+        ac = workloads.make_append_workload(name, seed=0, device=dev)
+        c = ac.case
+        n, d = ac.n_tokens, ac.d_model
+        copies = _l2_copies(ac.weight_bytes() + n * d * 2)
+        hs = [ac.h.clone() for _ in range(copies)]
+        wds = [ac.w_dkv.clone() for _ in range(copies)]
+        wrs = [ac.w_kr.clone() for _ in range(copies)]
+        bt, sl, pool = c.block_table.to(dev), c.seq_lens.to(dev), c.pool
+
+        def call(k):
+            return lambda st: mla.cache_append(hs[k], wds[k], wrs[k], bt, sl, pool, q_len=c.Tq, stream=st)
+        for i in range(max(warmup, copies)):
+            call(i % copies)(stream)
+        torch.cuda.synchronize()
+        n0 = mla.launch_count()
+        call(0)(stream)
+        launches = mla.launch_count() - n0
+        us = graph_us([call(k) for k in range(copies)], max(1, steps // copies))
+        bytes_ = ac.weight_bytes() + n * d * 2 + n * ROW_BYTES
+        flops = 2.0 * n * 576 * d
+        gbs = bytes_ / (us * 1e-6) / 1e9
+        tf = flops / (us * 1e-6) / 1e12
+        t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+        res[name] = {"tokens": n, "us": us, "bytes": bytes_, "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"],
+                     "tflops": tf, "frac_tensor": tf / pk["bf16_tflops"], "t_roof_us": t_roof * 1e6,
+                     "roofline_frac": t_roof / (us * 1e-6), "launches_per_call": launches, "copies": copies}
+        del hs, wds, wrs, ac, c, pool
+        torch.cuda.empty_cache()
+    st, word = mla.get_device_status()
+    assert st == 0, f"device status {word:#x}"
     return res
 
 
@@ -375,6 +465,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused absorb/decode/up-projection timing")
+    ap.add_argument("--no-append", action="store_true", help="skip the cache-write timing")
     ap.add_argument("--ref-seqs", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -513,6 +604,9 @@ def main():
     fused = None
     if rank == 0 and args.workload == "b64_l4096" and not args.no_fused:
         fused = fused_leg(mla, workloads, dev, stream, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks())
+    append = None
+    if rank == 0 and args.workload == "b64_l4096" and not args.no_append:
+        append = append_leg(mla, workloads, dev, stream, steps=max(args.steps, 20), warmup=args.warmup, pk=peaks())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -548,6 +642,7 @@ def main():
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "fused": fused,
+            "append": append,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -55,7 +55,9 @@ typedef enum {
 
 /* Bits of the device status word. */
 #define MLA_DEV_BAD_BLOCK_TABLE 0x1u  /* a block-table entry outside [0, num_pages) was read */
-#define MLA_DEV_BAD_SEQ_LEN     0x2u  /* a sequence length outside [0, max_pages * 64] */
+#define MLA_DEV_BAD_SEQ_LEN     0x2u  /* a sequence length outside [0, max_pages * 64], or (cache
+                                         write) a new token's position negative or past the
+                                         block table */
 #define MLA_DEV_WAIT_TIMEOUT    0x4u  /* an on-chip wait gave up (kernel bailed out) */
 #define MLA_DEV_PLAN_OVERFLOW   0x8u  /* the split plan did not fit the workspace */
 
@@ -171,10 +173,52 @@ mla_status_t mla_up_proj(const void *o_lat, const void *w_uv, void *out, int n_t
                          mla_stream_t stream);
 
 /*
+ * mla_cache_append - write the cache rows of new tokens, the step before the
+ * decode (explainer Step 5, the paper's equation 9: the hidden vector is
+ * projected down to the latent c = W^DKV h, 512 numbers; Step 7: the token's
+ * one position key shared by all heads is k^R = RoPE(W^KR h), 64 numbers;
+ * Step 8: the row kept is [c | k^R]):
+ *     row[n, 0:512]   = W^DKV h[n]                     (fp32 accumulate)
+ *     row[n, 512:576] = RoPE_pos(W^KR h[n])            (fp32, then the row to bf16)
+ *     kv_pool[block_table[b, pos / 64], pos % 64, :] = row[n]
+ * for token t of sequence b (n = b * q_len + t), at position
+ * pos = seq_lens[b] - q_len + t: the lengths already count the new tokens, as
+ * in mla_decode's causal mode.  A decode step is q_len = 1; a prefill of a
+ * prompt of L tokens is q_len = L with seq_lens = L.
+ *
+ * RoPE (the pages give no formula; the reading taken): coordinates (2i, 2i+1)
+ * of k^R form pair i, turned counter-clockwise by pos * rope_base^(-2i/64):
+ *     (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a).
+ *
+ * h            [batch * q_len, d_model] bf16, the new tokens' hidden vectors
+ * w_dkv        [512, d_model] bf16, row r gives c[r] = W^DKV[r,:] . h
+ * w_kr         [64, d_model] bf16, likewise for k^R before the rotation
+ * block_table  [batch, max_pages] int32, device; seq_lens [batch] int32, device
+ * rope_base    > 1 (10000 for DeepSeek-V2 shapes)
+ * kv_pool      [num_pages, 64, 576] bf16, written in place; only the rows of
+ *              the new tokens change.  The call needs no workspace.
+ * A token whose position is negative or beyond the block table, or whose page
+ * is outside [0, num_pages), is not written: the status word records
+ * MLA_DEV_BAD_SEQ_LEN or MLA_DEV_BAD_BLOCK_TABLE.  Two new tokens mapped to the
+ * same pool row race; the caller's block table must not do that.
+ * Limits: 1 <= batch * q_len <= 2^20; d_model a multiple of 64, at most 65536.
+ */
+mla_status_t mla_cache_append(const void *h, const void *w_dkv, const void *w_kr, const int32_t *block_table,
+                              const int32_t *seq_lens, int batch, int q_len, int d_model, int num_pages,
+                              int max_pages, float rope_base, void *kv_pool, mla_stream_t stream);
+
+/*
  * mla_get_device_status - synchronise `stream`, then read and clear the
  * library's device status word on the current device (MLA_DEV_* bits).
  * Returns MLA_ERR_DEVICE_FAULT if any bit was set, MLA_ERR_CUDA if the stream
  * reported an error, MLA_OK otherwise.  err_word may be NULL.
+ *
+ * There is one word per device, shared by every call, stream and host thread
+ * of the process on that device: kernels only ever set bits in it (atomic OR),
+ * and this call reads and clears it after synchronising `stream` alone.  A bit
+ * set by work on another stream may therefore be reported here, or missed if
+ * that work has not finished; callers that need per-stream attribution keep
+ * one stream per device, or synchronise the device before reading.
  */
 mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t *err_word);
 

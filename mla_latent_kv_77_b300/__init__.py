@@ -28,6 +28,7 @@ D_H = 128
 D = D_C + D_R
 PAGE = 64
 SCALE = 1.0 / math.sqrt(D_H + D_R)
+ROPE_BASE = 10000.0  # RoPE frequency base of the cache write (pair i turns at ROPE_BASE^(-2i/64) per position)
 
 # device status bits (MLA_DEV_* in mla.h)
 DEV_BAD_BLOCK_TABLE = 0x1
@@ -64,6 +65,7 @@ EXPORTS = {
     "mla_decode_static_scratch": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _VP, _VP]),
     "mla_combine": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP]),
     "mla_up_proj": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
+    "mla_cache_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _VP]),
     "mla_get_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "mla_cache_bytes": (ctypes.c_uint64, [ctypes.c_int64, _I, _I, _I, _I]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
@@ -154,6 +156,30 @@ def up_proj(o_lat, w_uv, out=None, stream=None):
     _check(lib().mla_up_proj(_ptr(o_lat), _ptr(w_uv), _ptr(out), n_tok, o_lat.shape[-2], _stream(stream)),
            "mla_up_proj")
     return out
+
+
+def cache_append(h, w_dkv, w_kr, block_table, seq_lens, kv_pool, q_len: int = 1, rope_base: float = ROPE_BASE,
+                 stream=None):
+    """Write the cache rows [W^DKV h | RoPE_pos(W^KR h)] of new tokens into the paged pool, in place.
+
+    h [B * q_len, d_model] (or [B, q_len, d_model]) bf16, w_dkv [512, d_model] bf16, w_kr [64, d_model]
+    bf16, block_table [B, max_pages] int32, seq_lens [B] int32 counting the new tokens (token t of
+    sequence b sits at position seq_lens[b] - q_len + t), kv_pool [P, 64, 576] bf16.  Returns kv_pool.
+    """
+    import torch
+    for t, n in ((h, "h"), (w_dkv, "w_dkv"), (w_kr, "w_kr"), (kv_pool, "kv_pool")):
+        _need(t, torch.bfloat16, n)
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B = block_table.shape[0]
+    d_model = h.shape[-1]
+    if h.numel() != B * q_len * d_model:
+        raise ValueError(f"h: expected {B} x {q_len} tokens of width {d_model}")
+    st = lib().mla_cache_append(_ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(block_table), _ptr(seq_lens), B,
+                                int(q_len), d_model, kv_pool.shape[0], block_table.shape[1], float(rope_base),
+                                _ptr(kv_pool), _stream(stream))
+    _check(st, "mla_cache_append")
+    return kv_pool
 
 
 def decode(q_abs, kv_pool, block_table, seq_lens, scale: float = SCALE, causal: bool = False,

@@ -55,14 +55,6 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t smem_src
                  "r"(smem_src), "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_nohint(uint32_t smem_dst, const void *tmap, int32_t x, int32_t y,
-                                                   int32_t z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -189,7 +181,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                 for (int u = 0; u < 8; ++u) dst[u] = src[u];
             }
         }
-        const bool ok = mbar_wait(bar(10), 0, abort);
+        // tcgen05.ld is warp-collective: the whole warp takes the same branch around it
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(10), 0, abort));
         if (ok) {
             tc_fence_after();
             // each accumulator -> bf16 -> shared tile [token][128 columns] (256-byte rows); a store

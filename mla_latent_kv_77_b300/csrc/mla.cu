@@ -1,6 +1,7 @@
 // mla.cu - C ABI of the MLA decode library (declared in include/mla.h).
 // Host side only: argument checks, TMA descriptors, launch configuration.
-// Every numeric step runs in the kernels of decode_kernels.cuh / gemm_kernels.cuh.
+// Every numeric step runs in the kernels of decode_kernels.cuh, gemm_kernels.cuh and
+// append_kernels.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -12,6 +13,7 @@
 
 #include "../../include/mla.h"
 #include "../../include/mla_testing.h"
+#include "append_kernels.cuh"
 #include "decode_kernels.cuh"
 #include "gemm_kernels.cuh"
 
@@ -21,6 +23,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRows = 65536;       // batch * q_len limit of the planner
 constexpr int kMaxQLen = 64;
+constexpr int kMaxAppendTokens = 1 << 20;  // new tokens per cache write (a long prefill)
+constexpr int kMaxDModel = 1 << 16;
 
 struct DeviceInfo {
     bool ready = false;
@@ -56,14 +60,21 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
             // SMs need not switch their L1 / shared split between the plan, decode and combine
             for (const void *fn : {(const void *)plan_kernel, (const void *)combine_kernel,
                                    (const void *)combine_rows_kernel, (const void *)decode_kernel,
-                                   (const void *)head_gemm_kernel})
+                                   (const void *)head_gemm_kernel, (const void *)append_kernel<64, 64>,
+                                   (const void *)append_kernel<64, 128>, (const void *)append_kernel<144, 128>})
                 cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
             cudaGetLastError();
             if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmem) !=
                     cudaSuccess ||
                 cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemMax) !=
-                    cudaSuccess)
+                    cudaSuccess ||
+                cudaFuncSetAttribute(append_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<64, 64>::kSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(append_kernel<64, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<64, 128>::kSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(append_kernel<144, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<144, 128>::kSmem) != cudaSuccess)
                 return MLA_ERR_CUDA;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
@@ -213,6 +224,36 @@ bool ws_layout(int batch, int q_len, int num_splits, WsLayout *w) {
     return true;
 }
 
+// Shape of the cache write for n_tokens new tokens: a few token tiles take 64-column tiles with K
+// split over a cluster of up to 8 CTAs (72 CTAs for one tile), loading only 64 rows of h when
+// there are at most 64 tokens; twelve or more token tiles fill the GPU by themselves and take
+// 144-column tiles without a split.  chunk = K blocks per TMA copy: about a fifth of a split's K
+// range, so the MMAs start on the first copy while the others land (all of them in flight when
+// the stages hold them); two for the prompt shape, whose long K loop runs on three stages.
+struct AppendConfig {
+    int bn, arows, splits, chunk;
+};
+AppendConfig append_config(int n_tokens, int d_model) {
+    const int tiles = (n_tokens + kAppendTileM - 1) / kAppendTileM;
+    const int nkb = d_model / 64;
+    if (tiles >= 12) return {144, 128, 1, nkb < 2 ? 1 : 2};
+    int s = 1;
+    while (2 * s <= kAppendMaxSplits && 2 * s * tiles <= kAppendMaxSplits && 2 * s <= nkb) s *= 2;
+    const int arows = n_tokens <= 64 ? 64 : 128;
+    const int nk_max = (nkb + s - 1) / s;
+    const int cap = arows == 64 ? AppendShape<64, 64>::kMaxChunk : AppendShape<64, 128>::kMaxChunk;
+    int c = (nk_max + 4) / 5;
+    if (c > cap) c = cap;
+    return {64, arows, s, c < 1 ? 1 : c};
+}
+
+// RoPE pair i turns by theta_i = base^(-2i/64) per position; as a fraction of a turn, theta_i / (2 pi)
+// < 1, held as an unsigned 64-bit binary fraction (exact in double: the value is below 2^62)
+uint64_t rope_turns(double base, int i) {
+    const double rate = std::pow(base, -2.0 * i / 64.0) / (2.0 * 3.14159265358979323846);
+    return (uint64_t)std::ldexp(rate, 64);
+}
+
 // One thread waits on a barrier that nothing completes; the bounded wait gives up.
 __global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -276,6 +317,78 @@ size_t mla_decode_workspace_size(int batch, int q_len, int num_splits) {
     WsLayout w;
     if (!ws_layout(batch, q_len, num_splits, &w)) return 0;
     return w.total;
+}
+
+mla_status_t mla_cache_append(const void *h, const void *w_dkv, const void *w_kr, const int32_t *block_table,
+                              const int32_t *seq_lens, int batch, int q_len, int d_model, int num_pages,
+                              int max_pages, float rope_base, void *kv_pool, mla_stream_t stream) {
+    if (!h || !w_dkv || !w_kr || !block_table || !seq_lens || !kv_pool) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || q_len < 1 || num_pages < 1 || max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+    const long long n_tokens = (long long)batch * q_len;
+    if (n_tokens > kMaxAppendTokens || d_model < 64 || d_model % 64 != 0 || d_model > kMaxDModel) return MLA_ERR_SHAPE;
+    if ((long long)num_pages * kPage > 0x7fffffffll || (long long)max_pages * kPage > 0x7fffffffll) return MLA_ERR_SHAPE;
+    if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(kv_pool) || !aligned4(block_table) ||
+        !aligned4(seq_lens))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    const AppendConfig cf = append_config((int)n_tokens, d_model);
+    const uint32_t nkb = (uint32_t)(d_model / 64);
+    CUtensorMap th, twa, twb, twr;
+    if (!tmap_col_blocks(&th, h, (uint64_t)n_tokens, nkb, (uint32_t)cf.arows, (uint32_t)cf.chunk) ||
+        !tmap_col_blocks(&twa, w_dkv, kAppendLatent, nkb, (uint32_t)cf.bn, (uint32_t)cf.chunk) ||
+        !tmap_col_blocks(&twr, w_kr, kAppendCols - kAppendLatent, nkb, kAppendCols - kAppendLatent,
+                         (uint32_t)cf.chunk))
+        return MLA_ERR_CUDA;
+    if (kAppendLatent % cf.bn == 0)
+        twb = twa;  // no column tile straddles the two matrices
+    else if (!tmap_col_blocks(&twb, w_dkv, kAppendLatent, nkb, (uint32_t)(kAppendLatent % cf.bn), (uint32_t)cf.chunk))
+        return MLA_ERR_CUDA;
+    AppendParams p;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.pool = static_cast<__nv_bfloat16 *>(kv_pool);
+    p.n_tokens = (int)n_tokens;
+    p.q_len = q_len;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.nkb = d_model / 64;
+    p.splits = cf.splits;
+    p.chunk = cf.chunk;
+    for (int i = 0; i < kAppendPairs; ++i) p.turns[i] = rope_turns((double)rope_base, i);
+    const unsigned token_tiles = (unsigned)((n_tokens + kAppendTileM - 1) / kAppendTileM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kAppendThreads, 1, 1);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cf.splits;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (cf.bn == 64 && cf.arows == 64) {
+        cfg.gridDim = dim3((unsigned)cf.splits, AppendShape<64, 64>::kColTiles, token_tiles);
+        cfg.dynamicSmemBytes = AppendShape<64, 64>::kSmem;
+        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 64>, th, twa, twb, twr, p);
+    } else if (cf.bn == 64) {
+        cfg.gridDim = dim3((unsigned)cf.splits, AppendShape<64, 128>::kColTiles, token_tiles);
+        cfg.dynamicSmemBytes = AppendShape<64, 128>::kSmem;
+        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 128>, th, twa, twb, twr, p);
+    } else {
+        cfg.gridDim = dim3(1, AppendShape<144, 128>::kColTiles, token_tiles);
+        cfg.dynamicSmemBytes = AppendShape<144, 128>::kSmem;
+        e = cudaLaunchKernelEx(&cfg, append_kernel<144, 128>, th, twa, twb, twr, p);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    return launch_error(1);
 }
 
 // 3-D bf16 view (cols, heads, tokens) of a [tokens, 128, cols] output for the GEMMs' TMA stores:

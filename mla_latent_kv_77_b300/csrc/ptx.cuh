@@ -37,7 +37,8 @@ struct Tracer {
     uint32_t n;
     __device__ __forceinline__ Tracer() : n(0) {
         uint64_t *b = g_trace;
-        p = b ? b + ((size_t)blockIdx.x * kTraceWarps + (threadIdx.x >> 5)) * kTraceSlots : nullptr;
+        const size_t block = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+        p = b ? b + (block * kTraceWarps + (threadIdx.x >> 5)) * kTraceSlots : nullptr;
     }
     __device__ __forceinline__ void at(uint32_t tag) {
         if (p != nullptr && (threadIdx.x & 31) == 0 && n < (uint32_t)kTraceSlots) {
@@ -79,6 +80,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The same rendezvous without ordering this thread's earlier memory writes: for a last barrier
+// whose only job is to keep a CTA's shared memory alive until its partners have read it (their
+// reads are complete once they have used the values), so the arrive need not wait for this
+// thread's global stores to be acknowledged.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
 }
 
 // ----------------------------------------------------------------------------
@@ -203,6 +211,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void *tmap,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+// 3-D tiled load without a cache hint
+__device__ __forceinline__ void tma_load_3d_nohint(uint32_t smem_dst, const void *tmap, int32_t x, int32_t y,
+                                                   int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
 

@@ -2,14 +2,18 @@
 without it).
 
   python -m mla_latent_kv_77_b300.trace [--workload NAME] [--out FILE.npz]
+  python -m mla_latent_kv_77_b300.trace --append NAME [--out FILE.npz]
 
 builds ``libmla_trace.so`` from the same sources with ``-DMLA_TRACE`` (every role of the decode
-kernel then stamps its waits and issues with the SM cycle counter, see ``Tracer`` in
-``csrc/ptx.cuh``), runs one ``mla_decode`` call of the workload with a trace buffer, saves the raw
-records and prints, per role, the median time of each wait and piece of work per page.
+and cache-write kernels then stamps its waits and issues with the SM cycle counter, see ``Tracer``
+in ``csrc/ptx.cuh``), runs one ``mla_decode`` (or ``mla_cache_append``) call of the workload with a
+trace buffer, saves the raw records and prints, per role, the median time of each wait and piece of
+work per page (for the cache write: each step's time since the CTA's setup, and the spread of the
+CTAs' start and end times).
 
 Record layout: [CTA][warp][slot] 64-bit words, tag in bits 48-63, SM cycles (or, for tags >=
-0x8000, the global nanosecond timer) in bits 0-47.  Even CTAs score, odd CTAs accumulate.
+0x8000, the global nanosecond timer) in bits 0-47; CTAs in linear block order.  In the decode,
+even CTAs score, odd CTAs accumulate.
 """
 from __future__ import annotations
 
@@ -85,6 +89,83 @@ def record(workload: str, out: str) -> str:
     return out
 
 
+def record_append(workload: str, out: str) -> str:
+    import torch
+    import mla_latent_kv_77_b300 as mla
+    from mla_latent_kv_77_b300 import workloads
+    if mla._lib is not None:
+        raise RuntimeError("the untraced library is already loaded in this process")
+    mla.LIB_PATH = TRACE_LIB
+    lib = mla.lib()
+    lib.mla_trace_set.restype = ctypes.c_int
+    lib.mla_trace_set.argtypes = [ctypes.c_void_p]
+    dev = torch.device("cuda")
+    ac = workloads.make_append_workload(workload, seed=0, device=dev)
+    c = ac.case
+    bt, sl = c.block_table.to(dev), c.seq_lens.to(dev)
+    buf = torch.zeros(148 * WARPS * SLOTS, dtype=torch.int64, device=dev)
+    for _ in range(3):
+        mla.cache_append(ac.h, ac.w_dkv, ac.w_kr, bt, sl, c.pool, q_len=c.Tq)
+    # fresh weights, as in a model's layer loop, so the traced call reads them from HBM
+    w_dkv, w_kr, h = ac.w_dkv.clone(), ac.w_kr.clone(), ac.h.clone()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush.fill_(1)
+    torch.cuda.synchronize()
+    if lib.mla_trace_set(ctypes.c_void_p(buf.data_ptr())) != 0:
+        raise RuntimeError("mla_trace_set failed")
+    mla.cache_append(h, w_dkv, w_kr, bt, sl, c.pool, q_len=c.Tq)
+    torch.cuda.synchronize()
+    lib.mla_trace_set(ctypes.c_void_p(0))
+    st, word = mla.get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {word:#x}")
+    np.savez_compressed(out, trace=buf.cpu().numpy(), workload=workload, kind="append")
+    return out
+
+
+# cache-write steps: (name, warp, tag); times since the warp's setup stamp (0x102)
+APPEND_STEPS = [
+    ("producer: every load issued", 0, 0x111),
+    ("producer: every load landed", 0, 0x112),
+    ("MMA: first stage landed", 1, 0x120),
+    ("MMA: last MMA issued", 1, 0x121),
+    ("epilogue: accumulator complete", 2, 0x130),
+    ("epilogue: partial staged", 2, 0x131),
+    ("epilogue: cluster partials visible", 2, 0x140),
+    ("epilogue: rows written", 2, 0x141),
+]
+
+
+def summarize_append(path: str, mhz: float = 2032.0) -> str:
+    d = np.load(path)
+    tr = d["trace"].reshape(148, WARPS, SLOTS)
+    ctas = [b for b in range(148) if (tr[b, 2] != 0).any()]
+    lines = [f"{path}: {len(ctas)} CTAs; medians (max) over them, us since the CTA's setup at {mhz:.0f} MHz"]
+    for name, warp, tag in APPEND_STEPS:
+        xs = []
+        for b in ctas:
+            tags, t = _events(tr, b, warp)
+            t0 = t[tags == 0x102]
+            t1 = t[tags == tag]
+            if t0.size and t1.size:
+                xs.append((t1[0] - t0[0]) / mhz)
+        if xs:
+            lines.append(f"  {name:40s} {np.median(xs):7.3f} ({np.max(xs):.3f})")
+    starts, ends = [], []
+    for b in ctas:
+        tags, t = _events(tr, b, 2)
+        if (tags == 0x8101).any() and (tags == 0x8142).any():
+            starts.append(t[tags == 0x8101][0])
+            ends.append(t[tags == 0x8142][0])
+    if starts:
+        t0 = min(starts)
+        s_ = (np.array(starts) - t0) / 1000.0
+        e_ = (np.array(ends) - t0) / 1000.0
+        lines.append(f"  CTA start (global timer, us after the first): median {np.median(s_):.3f} max {s_.max():.3f}")
+        lines.append(f"  CTA end: median {np.median(e_):.3f} max {e_.max():.3f}")
+    return "\n".join(lines)
+
+
 def _events(tr, cta, warp):
     x = tr[cta, warp]
     x = x[x != 0]
@@ -131,12 +212,19 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="b64_l4096")
     ap.add_argument("--out", default=None)
+    ap.add_argument("--append", default=None, help="trace the cache write on this workload instead")
     ap.add_argument("--summarize", default=None, help="only summarise an existing record")
     args = ap.parse_args()
     if args.summarize:
-        print(summarize(args.summarize))
+        kind = str(np.load(args.summarize).get("kind", "decode"))
+        print(summarize_append(args.summarize) if kind == "append" else summarize(args.summarize))
         return 0
     build()
+    if args.append:
+        out = args.out or f"trace_{args.append}.npz"
+        record_append(args.append, out)
+        print(summarize_append(out))
+        return 0
     out = args.out or f"trace_{args.workload}.npz"
     record(args.workload, out)
     print(summarize(out))

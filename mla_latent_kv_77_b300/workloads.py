@@ -19,6 +19,9 @@ reproducible on its own; the ragged lengths come first, from a generator seeded
        the bf16 rounding)
   --   optional garbage (NaN or 1e30) written into pool pages and tail slots that
        no sequence may read
+  k=9  h (cache write: the new tokens' hidden vectors) ~ N(0, 1), bf16
+  k=10 W^DKV        ~ N(0, 1) / sqrt(d_model), bf16   (so c ~ N(0, 1))
+  k=11 W^KR         ~ N(0, 1) / sqrt(d_model), bf16
 
 Shapes follow the DeepSeek-V2 attention: 128 heads, 512-d latent, 64-d decoupled
 RoPE key, 128-d head, 576-number cache row, 64-token pages.
@@ -38,6 +41,7 @@ D_H = 128
 D = D_C + D_R
 PAGE = 64
 SCALE = 1.0 / math.sqrt(D_H + D_R)
+D_MODEL = 5120  # DeepSeek-V2 hidden size: the cache write projects 5,120 numbers down to 512
 
 
 @dataclass
@@ -93,7 +97,7 @@ def make_case(name: str, seq_lens: List[int], Tq: int = 1, causal: bool = False,
     garbage      None, "nan" or "big": fill the unowned pages and the unused tail slots
                  of every sequence's last page with NaN or 1e30, to prove they are never read.
     peaked_frac  fraction of each sequence's rows multiplied by 8 (whole 576-wide row).
-    q_mode       "abs": draw q_abs; "nope": draw q_nope, q_rope, W_UK, W_UV; "both".
+    q_mode       "abs": draw q_abs; "nope": draw q_nope, q_rope, W_UK, W_UV; "both"; "none".
     """
     device = torch.device(device)
     B = len(seq_lens)
@@ -189,3 +193,50 @@ def make_workload(name: str, seed: int = 0, device="cpu") -> Case:
         B, lo, hi = spec.pop("ragged")
         spec["seq_lens"] = ragged_lengths(B, lo, hi, seed)
     return make_case(name, seed=seed, device=device, **spec)
+
+
+@dataclass
+class AppendCase:
+    """A cache write: Tq new tokens per sequence, already counted in the case's seq_lens."""
+    case: Case                      # the pool (prior content), block table, lengths
+    h: torch.Tensor                 # [B * Tq, d_model] bf16
+    w_dkv: torch.Tensor             # [D_C, d_model] bf16
+    w_kr: torch.Tensor              # [D_R, d_model] bf16
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.h.shape[0])
+
+    @property
+    def d_model(self) -> int:
+        return int(self.h.shape[1])
+
+    def weight_bytes(self) -> int:
+        return (D_C + D_R) * self.d_model * 2
+
+
+def make_append_case(name: str, seq_lens: List[int], Tq: int = 1, d_model: int = D_MODEL,
+                     shuffle: bool = False, spare_pages: int = 0, garbage: Optional[str] = None,
+                     seed: int = 0, device="cpu") -> AppendCase:
+    """A pool as make_case builds it, plus the new tokens' hidden vectors and the two weights."""
+    case = make_case(name, seq_lens, Tq=Tq, causal=True, shuffle=shuffle, spare_pages=spare_pages,
+                     garbage=garbage, q_mode="none", seed=seed, device=device)
+    h = _randn_bf16((len(seq_lens) * Tq, d_model), 1.0, seed, 9, device)
+    w_dkv = _randn_bf16((D_C, d_model), 1.0 / math.sqrt(d_model), seed, 10, device)
+    w_kr = _randn_bf16((D_R, d_model), 1.0 / math.sqrt(d_model), seed, 11, device)
+    return AppendCase(case=case, h=h, w_dkv=w_dkv, w_kr=w_kr)
+
+
+# Cache-write workloads: one decode step's new tokens at the decode workloads' batches, and a prefill.
+APPEND_WORKLOADS = {
+    # batch 64, one new token each after 4095 cached (the batch-64, 4096-token decode step)
+    "append_b64_l4096": dict(seq_lens=[4096] * 64, Tq=1),
+    # batch 32, four new tokens each after 8192 cached (the fused causal workload's step)
+    "append_b32_tq4": dict(seq_lens=[8192 + 4] * 32, Tq=4),
+    # one 4096-token prompt written at once (the prefill form)
+    "prefill_l4096": dict(seq_lens=[4096], Tq=4096),
+}
+
+
+def make_append_workload(name: str, seed: int = 0, device="cpu") -> AppendCase:
+    return make_append_case(name, seed=seed, device=device, **APPEND_WORKLOADS[name])

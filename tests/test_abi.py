@@ -119,6 +119,42 @@ def test_absorb_and_up_proj_reject_bad_arguments_on_host(lib):
     assert lib.mla_test_bounded_wait(0, None) == mla.Status.INVALID_ARG
 
 
+def _append_args(**over):
+    a = dict(h=16, wd=32, wr=48, bt=64, sl=80, B=2, Tq=1, d=5120, P=4, maxp=2, base=10000.0, pool=96)
+    a.update(over)
+    return a
+
+
+def _call_append(lib, a):
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    return lib.mla_cache_append(vp(a["h"]), vp(a["wd"]), vp(a["wr"]), vp(a["bt"]), vp(a["sl"]), a["B"], a["Tq"],
+                                a["d"], a["P"], a["maxp"], a["base"], vp(a["pool"]), None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(h=None), mla.Status.INVALID_ARG),
+    (dict(wd=None), mla.Status.INVALID_ARG),
+    (dict(wr=None), mla.Status.INVALID_ARG),
+    (dict(bt=None), mla.Status.INVALID_ARG),
+    (dict(sl=None), mla.Status.INVALID_ARG),
+    (dict(pool=None), mla.Status.INVALID_ARG),
+    (dict(B=0), mla.Status.INVALID_ARG),
+    (dict(Tq=0), mla.Status.INVALID_ARG),
+    (dict(P=0), mla.Status.INVALID_ARG),
+    (dict(maxp=0), mla.Status.INVALID_ARG),
+    (dict(base=1.0), mla.Status.INVALID_ARG),
+    (dict(base=float("inf")), mla.Status.INVALID_ARG),
+    (dict(d=5000), mla.Status.SHAPE),
+    (dict(d=0), mla.Status.SHAPE),
+    (dict(B=1 << 11, Tq=1 << 10), mla.Status.SHAPE),
+    (dict(h=24), mla.Status.ALIGNMENT),
+    (dict(pool=8), mla.Status.ALIGNMENT),
+    (dict(bt=66), mla.Status.ALIGNMENT),
+])
+def test_cache_append_rejects_bad_arguments_on_host(lib, over, code):
+    assert _call_append(lib, _append_args(**over)) == code
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mla, "_lib", None)
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
