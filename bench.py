@@ -15,7 +15,6 @@ collective on the data path; the barrier and max-over-ranks only bracket the tim
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -53,9 +52,16 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of what the decode launch is built from: the decode kernels, the PTX wrappers they
+    use, and mla_decode's launch code in mla.cu (the rest of mla.cu serves other calls)."""
+    csrc = os.path.join(ROOT, "mla_latent_kv_77_b300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_77_b300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in ("decode_kernels.cuh", "ptx.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    host = open(os.path.join(csrc, "mla.cu"), "rb").read()
+    a = host.find(b"mla_status_t mla_decode(")
+    b = host.find(b"mla_status_t mla_decode_static_scratch(")
+    h.update(host[a:b] if 0 <= a < b else host)
     return h.hexdigest()[:16]
 
 
