@@ -450,6 +450,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // any lane gave up, the whole warp gives up together.
 #define MLA_WAIT_WARP(bar_, par_, ab_) \
     if (__any_sync(0xffffffffu, !mbar_wait(bar_, par_, ab_))) return
+// The same all-lane wait, returning the outcome.  The single-thread roles below (shipper, P
+// loader, releaser) run as whole warps for it: a lone waiting thread measured a much slower
+// wake-up than a converged warp waiting together (about 6% of a batch-64 decode call when the
+// page producers and the PV warp waited on one lane).
+template <bool kCluster = false>
+__device__ __forceinline__ bool all_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    return !__any_sync(0xffffffffu, !mbar_wait<kCluster>(bar, parity, abort));
+}
 
 // Page ids of an item, read from the block table 32 tiles at a time (one per lane), one chunk
 // ahead of use.
@@ -498,7 +506,7 @@ __device__ __forceinline__ void value_producer_loop(const DecodeParams &p, const
             const int pg = ids.get(p, it, tile, lane);
             const uint32_t s = u % kStagesV;
             tr.at(0x50);
-            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesV) & 1u) ^ 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarEmpty + s), ((u / kStagesV) & 1u) ^ 1u, abort);
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageV);
                 tma_load_3d(sm.stage(s, kStageV), tmap, 0, pg * kPage, 0, sm.bar(kBarFull + s), pol);
@@ -534,7 +542,7 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
         for (int hq = 0; hq < 2; ++hq, ++u) {
             const uint32_t s = u % kStagesS;
             tr.at(0x12);
-            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort);
             tr.at(0x13);
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
@@ -549,7 +557,7 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
             const int pg = ids.get(p, it, tile, lane);
             const uint32_t s = u % kStagesS;
             tr.at(0x10);
-            if (!warp_wait(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarEmpty + s), ((u / kStagesS) & 1u) ^ 1u, abort);
             tr.at(0x11);
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
@@ -870,7 +878,7 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
     }
 }
 
-// Score CTA, shipper (one thread): publishes the messages the softmax warps have written to
+// Score CTA, shipper (a warp that waits together; lane 0 acts): publishes the messages the softmax warps have written to
 // the partner.  It waits for the oldest unpublished message, takes the later ones of the same
 // item that are already complete (up to kMaxBatch), and publishes them together: one
 // cluster-scope release fence, then a relaxed remote arrival per message.  The fence waits
@@ -880,45 +888,53 @@ __device__ __forceinline__ void role_softmax(const DecodeParams &p, const Smem &
 // and the fence is cumulative, so the partner's acquire sees every row.
 __device__ __forceinline__ void role_shipper(const DecodeParams &p, const Smem &sm, const Sched &sc,
                                              volatile int *abort, Tracer &tr) {
+    const bool lead = (threadIdx.x & 31) == 0;
     uint32_t g = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         const uint32_t end = g + (uint32_t)(it.te > it.tb ? it.te - it.tb : 0);
         while (g < end) {
             tr.at(0x40);
-            if (!mbar_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
+            if (!all_wait(sm.bar(kBarPStaged + g % kRing), (g / kRing) & 1u, abort)) return;
             tr.at(0x41);
             uint32_t n = 1;
-            while (g + n < end && n < (uint32_t)kMaxBatch &&
-                   mbar_test(sm.bar(kBarPStaged + (g + n) % kRing), ((g + n) / kRing) & 1u))
-                ++n;
-            fence_acq_rel_cluster();
-            for (uint32_t k = 0; k < n; ++k)
-                mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPReady + (g + k) % kRing), 1));
+            if (lead) {
+                while (g + n < end && n < (uint32_t)kMaxBatch &&
+                       mbar_test(sm.bar(kBarPStaged + (g + n) % kRing), ((g + n) / kRing) & 1u))
+                    ++n;
+                fence_acq_rel_cluster();
+                for (uint32_t k = 0; k < n; ++k)
+                    mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPReady + (g + k) % kRing), 1));
+            }
+            n = __shfl_sync(0xffffffffu, n, 0);
             tr.at(0x4200 + n);
             g += n;
         }
     }
 }
 
-// Accumulate CTA, releaser (one thread): hands each ring slot back to the partner as soon as
+// Accumulate CTA, releaser (a warp that waits together; lane 0 acts): hands each ring slot back to the partner as soon as
 // its message has landed in shared memory, off the MMA warp's path.  Its local arrival is
 // the second one each P buffer needs before the loader refills it, so this thread can never
 // fall a whole buffer cycle behind the barrier it watches.
 __device__ __forceinline__ void role_releaser(const DecodeParams &p, const Smem &sm, const Sched &sc,
                                               volatile int *abort) {
+    const bool lead = (threadIdx.x & 31) == 0;
     uint32_t g = 0;
     ItemInfo it;
     for (int r = 0; sc.get(p, r, it); ++r) {
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
-            if (!mbar_wait(sm.bar(kBarPFull + g % kPBufs), (g / kPBufs) & 1u, abort)) return;
-            mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPFree + g % kRing), 0));
-            mbar_arrive(sm.bar(kBarPBufFree + g % kPBufs));
+            if (!all_wait(sm.bar(kBarPFull + g % kPBufs), (g / kPBufs) & 1u, abort)) return;
+            if (lead) {
+                mbar_arrive_cluster_relaxed(mapa_shared(sm.bar(kBarPFree + g % kRing), 0));
+                mbar_arrive(sm.bar(kBarPBufFree + g % kPBufs));
+            }
+            __syncwarp();
         }
     }
 }
 
-// Accumulate CTA, P loader (one thread): ring slot -> shared P buffer, as soon as the
+// Accumulate CTA, P loader (a warp that waits together; lane 0 copies): ring slot -> shared P buffer, as soon as the
 // partner has published it and the buffer's previous message has been used.
 __device__ __forceinline__ void p_loader_loop(const DecodeParams &p, const Smem &sm, const Sched &sc,
                                               volatile int *abort, uint32_t &g, Tracer &tr) {
@@ -929,15 +945,18 @@ __device__ __forceinline__ void p_loader_loop(const DecodeParams &p, const Smem 
         for (int tile = it.tb; tile < it.te; ++tile, ++g) {
             const uint32_t rs = g % kRing, jp = g % kPBufs;
             tr.at(0x60);
-            if (!mbar_wait<true>(sm.bar(kBarPReady + rs), (g / kRing) & 1u, abort)) return;
+            if (!all_wait<true>(sm.bar(kBarPReady + rs), (g / kRing) & 1u, abort)) return;
             tr.at(0x61);
             fence_proxy_async_global();  // the partner's writes, before our async-proxy reads
-            if (!mbar_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
+            if (!all_wait(sm.bar(kBarPBufFree + jp), ((g / kPBufs) & 1u) ^ 1u, abort)) return;
             tr.at(0x62);
-            mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
-            // P and its factors are contiguous in both places: one copy (the copy engine's cost
-            // per transfer is high)
-            bulk_load_g2s(sm.pbuf(jp), ring + (size_t)rs * kMsgBytes, kMsgBytes, sm.bar(kBarPFull + jp), keep);
+            if ((threadIdx.x & 31) == 0) {
+                mbar_arrive_expect_tx(sm.bar(kBarPFull + jp), kMsgBytes);
+                // P and its factors are contiguous in both places: one copy (the copy engine's
+                // cost per transfer is high)
+                bulk_load_g2s(sm.pbuf(jp), ring + (size_t)rs * kMsgBytes, kMsgBytes, sm.bar(kBarPFull + jp), keep);
+            }
+            __syncwarp();
         }
     }
 }
@@ -946,8 +965,10 @@ __device__ __forceinline__ void role_p_loader(const DecodeParams &p, const Smem 
                                               volatile int *abort, Tracer &tr) {
     uint32_t g = 0;
     p_loader_loop(p, sm, sc, abort, g, tr);
-    for (uint32_t k = (g > (uint32_t)kPBufs ? g - kPBufs : 0); k < g; ++k)
-        if (!mbar_wait_drain(sm.bar(kBarPFull + k % kPBufs), (k / kPBufs) & 1u)) break;
+    if ((threadIdx.x & 31) == 0)
+        for (uint32_t k = (g > (uint32_t)kPBufs ? g - kPBufs : 0); k < g; ++k)
+            if (!mbar_wait_drain(sm.bar(kBarPFull + k % kPBufs), (k / kPBufs) & 1u)) break;
+    __syncwarp();
 }
 
 // Accumulate CTA, MMA warp: O += P V, two N = 256 halves, K = 64 in 4 steps.  It also
@@ -968,7 +989,7 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
             const bool first = tile == it.tb, last = tile == it.te - 1;
             const uint32_t valid = (uint32_t)min(kPage, it.n_vis - tile * kPage);
             tr.at(0x70);
-            if (!warp_wait(sm.bar(kBarPFull + jp), (g / kPBufs) & 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarPFull + jp), (g / kPBufs) & 1u, abort);
             tr.at(0x71);
             const uint32_t mt = sm.meta(jp);
             if (first) {
@@ -1005,7 +1026,7 @@ __device__ __forceinline__ void accum_mma_loop(const DecodeParams &p, const Smem
             }
             const uint64_t a0 = sdesc_sw128(sm.pbuf(jp), 16u, 1024u);
             const uint32_t s = g % kStagesV;
-            if (!warp_wait(sm.bar(kBarFull + s), (g / kStagesV) & 1u, abort)) return;
+            MLA_WAIT_WARP(sm.bar(kBarFull + s), (g / kStagesV) & 1u, abort);
             tr.at(0x74);
             const uint32_t vb = sm.stage(s, kStageV);
             if (last && valid < (uint32_t)kPage) {
@@ -1268,7 +1289,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
     sc.n_items = p.hdr->n_items;
     sc.first = load_item(p, sc.cid < p.max_items ? sc.cid : 0);  // needed only if cid < n_items
 
-    const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp < 8) {
         if (rank == 0)
             role_softmax(p, sm, tmem, sc, abort, tr);
@@ -1286,12 +1306,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
         } else if (warp == kWarpMma) {
             role_accum_mma(p, sm, tmem, sc, abort, tr);
         } else if (warp == kWarpMma + 1) {
-            if (lane0) role_p_loader(p, sm, sc, abort, tr);
+            role_p_loader(p, sm, sc, abort, tr);
         } else {
-            if (lane0) role_releaser(p, sm, sc, abort);
+            role_releaser(p, sm, sc, abort);
         }
     } else if (warp == kWarpShipper) {
-        if (rank == 0 && lane0) role_shipper(p, sm, sc, abort, tr);
+        if (rank == 0) role_shipper(p, sm, sc, abort, tr);
     }
     tr.at(0x03);
 
