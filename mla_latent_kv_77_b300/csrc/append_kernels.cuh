@@ -235,12 +235,14 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
     int pre_pos = 0;
     __nv_bfloat16 *pre_dst = nullptr;
 
+    // the producer and MMA roles run as whole warps that wait together (a lone waiting thread
+    // wakes up late); lane 0 issues the copies and the MMAs
     if (warp == 0) {
-        if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < n_chunks; ++i, ++issued) {
-                const int s = i % n_stages;
-                if (!mbar_wait(bar(S::kMaxStages + s), ((i / n_stages) & 1) ^ 1, abort)) break;
+        int issued = 0;
+        for (int i = 0; i < n_chunks; ++i, ++issued) {
+            const int s = i % n_stages;
+            if (__any_sync(0xffffffffu, !mbar_wait(bar(S::kMaxStages + s), ((i / n_stages) & 1) ^ 1, abort))) break;
+            if (lane == 0) {
                 const uint32_t sb = base + s * stage_bytes;
                 const int kbx = kb0 + i * C;
                 // a box reaching past n_tokens, past d_model or past this split's K range still
@@ -253,25 +255,28 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
                     b += (uint32_t)C * seg[g].rows * 128u;
                 }
             }
-            tr.at(0x111);
-            // wait for the last loads (normal exit or abort) before the CTA may move on
+            __syncwarp();
+        }
+        tr.at(0x111);
+        // wait for the last loads (normal exit or abort) before the CTA may move on
+        if (lane == 0)
             for (int k = issued > n_stages ? issued - n_stages : 0; k < issued; ++k)
                 if (!mbar_wait_drain(bar(k % n_stages), (k / n_stages) & 1)) break;
-            tr.at(0x112);
-        }
+        __syncwarp();
+        tr.at(0x112);
     } else if (warp == 1) {
-        if (lane == 0) {
-            uint32_t idesc[2];
-            for (int g = 0; g < n_seg; ++g) idesc[g] = idesc_bf16_f32(128, (uint32_t)seg[g].rows, 0, 0);
-            for (int i = 0; i < n_chunks; ++i) {
-                const int s = i % n_stages;
-                if (!mbar_wait(bar(s), (i / n_stages) & 1, abort)) break;
-                if (i == 0) tr.at(0x120);
-                tc_fence_after();
+        uint32_t idesc[2];
+        for (int g = 0; g < n_seg; ++g) idesc[g] = idesc_bf16_f32(128, (uint32_t)seg[g].rows, 0, 0);
+        for (int i = 0; i < n_chunks; ++i) {
+            const int s = i % n_stages;
+            if (__any_sync(0xffffffffu, !mbar_wait(bar(s), (i / n_stages) & 1, abort))) break;
+            if (i == 0) tr.at(0x120);
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t sb = base + s * stage_bytes;
                 const int nb = min(C, nk - i * C);
-                // descriptors of the chunk's first block; a block further on adds its byte offset / 16
-                // to the start-address field, a 16-wide K step adds 2
+                // descriptors of the chunk's first block; a block further on adds its byte offset
+                // / 16 to the start-address field, a 16-wide K step adds 2
                 const uint64_t a0 = sdesc_sw128(sb, 16u, 1024u);
                 uint64_t b0[2];
                 uint32_t off = a_bytes;
@@ -292,12 +297,16 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
                 }
                 mma_commit(bar(S::kMaxStages + s));
             }
-            tr.at(0x121);
+            __syncwarp();
+        }
+        tr.at(0x121);
+        if (lane == 0) {
             mma_commit(bar(kBarAcc));
             // every MMA issued has completed before the CTA may free its tensor memory
             mma_commit(bar(kBarDrain));
             mbar_wait_drain(bar(kBarDrain), 0);
         }
+        __syncwarp();
     } else {
         // epilogue: warps 2..5 -> TMEM lane quadrants 2, 3, 0, 1; lane = token row of the tile
         const int q = warp & 3;

@@ -428,15 +428,6 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-__device__ __forceinline__ int checked_page(const DecodeParams &p, int b, int tile) {
-    int pg = p.block_table[(size_t)b * p.max_pages + tile];
-    if (pg < 0 || pg >= p.num_pages) {
-        raise_status(0x1u);
-        pg = 0;
-    }
-    return pg;
-}
-
 // Waits whose lanes must stay converged (warp-collective instructions follow): lane 0 waits,
 // the outcome is broadcast, and on a failed wait the whole warp leaves together.
 template <bool kCluster = false>
@@ -460,22 +451,32 @@ __device__ __forceinline__ bool all_wait(uint32_t bar, uint32_t parity, volatile
 }
 
 // Page ids of an item, read from the block table 32 tiles at a time (one per lane), one chunk
-// ahead of use.
+// ahead of use.  The entries are loaded raw and checked when a page is taken, so start() only
+// issues the loads: a caller can start them before other work without waiting for them.
 struct PageIds {
     int cur, nxt, chunk;
+    __device__ __forceinline__ static int raw(const DecodeParams &p, int b, int tile) {
+        return p.block_table[(size_t)b * p.max_pages + tile];
+    }
     __device__ __forceinline__ void start(const DecodeParams &p, const ItemInfo &it, int lane) {
         chunk = it.tb;
-        cur = it.tb + lane < it.te ? checked_page(p, it.b, it.tb + lane) : 0;
-        nxt = it.tb + 32 + lane < it.te ? checked_page(p, it.b, it.tb + 32 + lane) : 0;
+        cur = it.tb + lane < it.te ? raw(p, it.b, it.tb + lane) : 0;
+        nxt = it.tb + 32 + lane < it.te ? raw(p, it.b, it.tb + 32 + lane) : 0;
     }
-    // page of `tile` (tiles visited in order); warp-collective
+    // page of `tile` (tiles visited in order); warp-collective.  An entry outside [0, num_pages)
+    // sets MLA_DEV_BAD_BLOCK_TABLE and reads page 0 instead.
     __device__ __forceinline__ int get(const DecodeParams &p, const ItemInfo &it, int tile, int lane) {
         if (tile - chunk == 32) {
             chunk += 32;
             cur = nxt;
-            nxt = chunk + 32 + lane < it.te ? checked_page(p, it.b, chunk + 32 + lane) : 0;
+            nxt = chunk + 32 + lane < it.te ? raw(p, it.b, chunk + 32 + lane) : 0;
         }
-        return __shfl_sync(0xffffffffu, cur, tile - chunk);
+        int pg = __shfl_sync(0xffffffffu, cur, tile - chunk);
+        if (pg < 0 || pg >= p.num_pages) {
+            if (lane == 0) raise_status(0x1u);
+            pg = 0;
+        }
+        return pg;
     }
 };
 
@@ -539,6 +540,7 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
     for (int r = 0; sc.get(p, r, it); ++r) {
         if (it.te <= it.tb) continue;
         const int row0 = it.bt * kHeads;
+        ids.start(p, it, lane);  // only issues the block-table loads; they land during the query's
         for (int hq = 0; hq < 2; ++hq, ++u) {
             const uint32_t s = u % kStagesS;
             tr.at(0x12);
@@ -552,7 +554,6 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
             }
             __syncwarp();
         }
-        ids.start(p, it, lane);  // the block table is read once the query's loads are on their way
         for (int tile = it.tb; tile < it.te; ++tile, ++u) {
             const int pg = ids.get(p, it, tile, lane);
             const uint32_t s = u % kStagesS;

@@ -111,12 +111,14 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // the producer and MMA roles run as whole warps that wait together (a lone waiting thread
+    // wakes up late); lane 0 issues the copies and the MMAs
     if (warp == 0) {
-        if (lane == 0) {
-            uint32_t issued = 0;
-            for (int kc = 0; kc < nk; ++kc, ++issued) {
-                const int s = kc % stages;
-                if (!mbar_wait(bar(5 + s), ((kc / stages) & 1) ^ 1, abort)) break;
+        uint32_t issued = 0;
+        for (int kc = 0; kc < nk; ++kc, ++issued) {
+            const int s = kc % stages;
+            if (__any_sync(0xffffffffu, !mbar_wait(bar(5 + s), ((kc / stages) & 1) ^ 1, abort))) break;
+            if (lane == 0) {
                 const uint32_t a = base + s * stage_bytes;
                 mbar_arrive_expect_tx(bar(s), stage_bytes);
                 if (absorb) {
@@ -133,17 +135,20 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                     tma_load_2d(a + kGemmTileBytes, &tmap_x, h * 512 + kc * 64, nt * kGemmTileN, bar(s));
                 }
             }
-            // wait for the last loads (normal exit or abort) before the CTA may move on
+            __syncwarp();
+        }
+        // wait for the last loads (normal exit or abort) before the CTA may move on
+        if (lane == 0)
             for (uint32_t k = issued > (uint32_t)stages ? issued - stages : 0; k < issued; ++k)
                 if (!mbar_wait_drain(bar(k % stages), (k / stages) & 1)) break;
-        }
+        __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = absorb ? idesc_bf16_f32(128, 128, 1, 0) : idesc_bf16_f32(128, 128, 0, 0);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % stages;
-                if (!mbar_wait(bar(s), (kc / stages) & 1, abort)) break;
-                tc_fence_after();
+        const uint32_t idesc = absorb ? idesc_bf16_f32(128, 128, 1, 0) : idesc_bf16_f32(128, 128, 0, 0);
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % stages;
+            if (__any_sync(0xffffffffu, !mbar_wait(bar(s), (kc / stages) & 1, abort))) break;
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t a = base + s * stage_bytes;
                 const uint32_t b = a + (absorb ? (uint32_t)kAbsorbAcc : 1u) * kGemmTileBytes;
                 for (int mc = 0; mc < n_acc; ++mc) {
@@ -159,11 +164,15 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                 }
                 mma_commit(bar(5 + s));
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             mma_commit(bar(10));
             // every MMA issued has completed before the CTA may free its tensor memory
             mma_commit(bar(13));
             mbar_wait_drain(bar(13), 0);
         }
+        __syncwarp();
     } else {
         // epilogue: warps 2..5 -> TMEM lane quadrants 2, 3, 0, 1; lane = weight-side index m
         const int q = warp & 3;
