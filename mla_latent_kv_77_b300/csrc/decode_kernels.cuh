@@ -231,6 +231,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int B, int Tq, int causal, int max_pages,
             int n_clusters, int num_splits, PlanHeader *hdr, Item *items, BtInfo *info,
             int *scratch /* 4 * B * Tq ints, used when B * Tq > kPlanSmemBt */, int max_items, int max_slots) {
+    // launched as a programmatic dependent of its predecessor (often the previous call's
+    // combine kernel, which lets it get resident early): nothing is read or written before that
+    // predecessor has completed -- it may have written seq_lens, or still read this workspace
+    grid_dependency_wait();
     grid_launch_dependents();  // the decode kernel may start its prologue while the plan is made
     __shared__ int s_tmp[32];
     __shared__ int s_key[kPlanThreads];
@@ -1376,7 +1380,8 @@ __device__ __forceinline__ void combine_row(const float *o_base, size_t o_stride
 __global__ void __launch_bounds__(128)
 combine_kernel(const PlanHeader *__restrict__ hdr, const BtInfo *__restrict__ info, const float *__restrict__ part_o,
                const float *__restrict__ part_lse, __nv_bfloat16 *__restrict__ o_lat, float *__restrict__ lse) {
-    grid_dependency_wait();  // launched as a programmatic dependent of the decode kernel
+    grid_launch_dependents();  // a following call's plan kernel may get resident; it waits for us
+    grid_dependency_wait();    // launched as a programmatic dependent of the decode kernel
     if (hdr->n_split == 0) return;
     const int n_units = hdr->n_bt * (kHeads / 8);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {

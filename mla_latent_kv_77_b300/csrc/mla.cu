@@ -497,10 +497,25 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     // one thread per query up to kPlanThreads (the rank sort wants that), in whole warps, at
     // least four: a small batch plans with few threads and few warps to synchronise
     const int plan_threads = n_bt >= kPlanThreads ? kPlanThreads : (n_bt <= 128 ? 128 : (n_bt + 31) / 32 * 32);
-    plan_kernel<<<1, plan_threads, 0, s>>>(seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
-                                           num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch),
-                                           w.max_items, w.max_slots);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    {
+        // a programmatic dependent of whatever precedes it (it waits for that to complete before
+        // reading anything): its launch overlaps the previous call's combine kernel
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(1, 1, 1);
+        pcfg.blockDim = dim3((unsigned)plan_threads, 1, 1);
+        pcfg.stream = s;
+        cudaLaunchAttribute pat[1];
+        pat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pat[0].val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = pat;
+        pcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&pcfg, plan_kernel, seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
+                               num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch), w.max_items,
+                               w.max_slots) != cudaSuccess) {
+            cudaGetLastError();
+            return MLA_ERR_CUDA;
+        }
+    }
 
     DecodeParams p;
     p.q_abs = static_cast<const __nv_bfloat16 *>(q_abs);
