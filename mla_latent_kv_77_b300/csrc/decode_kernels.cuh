@@ -482,6 +482,13 @@ struct PageIds {
         }
         return pg;
     }
+    // raw entry of a tile at most 32 ahead of the last one taken (no check); warp-collective
+    __device__ __forceinline__ int peek(int tile) {
+        const int d = tile - chunk;
+        const int a = __shfl_sync(0xffffffffu, cur, d & 31);
+        const int b = __shfl_sync(0xffffffffu, nxt, d & 31);
+        return d < 32 ? a : b;
+    }
 };
 
 // Accumulate CTA, page producer (a whole warp; lane 0 issues): one box per page, its 512 latent
@@ -567,6 +574,15 @@ __device__ __forceinline__ void score_producer_loop(const DecodeParams &p, const
             if (lane == 0) {
                 mbar_arrive_expect_tx(sm.bar(kBarFull + s), kStageS);
                 tma_load_3d(sm.stage(s, kStageS), pages, 0, pg * kPage, 0, sm.bar(kBarFull + s), keep);
+            }
+            {
+                // the next page, when it does not follow this one in the pool, is prefetched into
+                // L2 now: on a randomly paged pool that measured about 5% faster; for pages in
+                // pool order the prefetch cost more than it saved, so none is issued
+                const int t2 = tile + 1;
+                const int pg2 = ids.peek(t2);
+                if (lane == 0 && t2 < it.te && pg2 >= 0 && pg2 < p.num_pages && pg2 != pg + 1)
+                    tma_prefetch_l2_3d(pages, 0, pg2 * kPage, 0);
             }
             __syncwarp();
         }

@@ -213,6 +213,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
+// the box of a 3-D tensor map at (x, y, z), fetched into L2 only
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 // 3-D tiled load without a cache hint
 __device__ __forceinline__ void tma_load_3d_nohint(uint32_t smem_dst, const void *tmap, int32_t x, int32_t y,
                                                    int32_t z, uint32_t bar) {
