@@ -1354,73 +1354,88 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant_
 // ---------------------------------------------------------------------------
 // LSE combine: merge the partials of queries that were split.
 // ---------------------------------------------------------------------------
-// thread block = 8 heads x 16 threads, each thread 32 latent columns
+// The LSE merge of one (query, head) row's partial results, by 64 threads taking 8 columns each.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineHeads = kCombineThreads / 64;  // rows per block
 __device__ __forceinline__ void combine_row(const float *o_base, size_t o_stride, const float *lse_base,
                                             size_t lse_stride, int n_parts, int col0, __nv_bfloat16 *o_out,
                                             float *lse_out, bool write_lse) {
+    // lse = log sum_r exp(lse_r), taken about the largest; the 64 threads of a row read the
+    // same lse values (one line, from L1)
     float mx = -INFINITY;
     for (int r = 0; r < n_parts; ++r) mx = fmaxf(mx, lse_base[r * lse_stride]);
-    float acc[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     float L = -INFINITY;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
     if (mx != -INFINITY) {
         float tot = 0.f;
         for (int r = 0; r < n_parts; ++r) tot += expf(lse_base[r * lse_stride] - mx);
         L = mx + logf(tot);
-        for (int r = 0; r < n_parts; ++r) {
-            const float w = expf(lse_base[r * lse_stride] - L);
-            if (w == 0.f) continue;
-            const float4 *src = reinterpret_cast<const float4 *>(o_base + r * o_stride + col0);
+        // eight parts at a time, all their loads in flight before any is used; a part whose
+        // weight is 0 (lse = -inf) is left out, whatever its output holds
+        for (int r0 = 0; r0 < n_parts; r0 += 8) {
+            float w[8];
+            float4 x0[8], x1[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float4 x = src[u];
-                acc[4 * u + 0] = fmaf(w, x.x, acc[4 * u + 0]);
-                acc[4 * u + 1] = fmaf(w, x.y, acc[4 * u + 1]);
-                acc[4 * u + 2] = fmaf(w, x.z, acc[4 * u + 2]);
-                acc[4 * u + 3] = fmaf(w, x.w, acc[4 * u + 3]);
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < n_parts) {
+                    w[j] = expf(lse_base[(r0 + j) * lse_stride] - L);
+                    const float4 *src = reinterpret_cast<const float4 *>(o_base + (r0 + j) * o_stride + col0);
+                    x0[j] = src[0];
+                    x1[j] = src[1];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < n_parts && w[j] != 0.f) {
+                    a0.x = fmaf(w[j], x0[j].x, a0.x);
+                    a0.y = fmaf(w[j], x0[j].y, a0.y);
+                    a0.z = fmaf(w[j], x0[j].z, a0.z);
+                    a0.w = fmaf(w[j], x0[j].w, a0.w);
+                    a1.x = fmaf(w[j], x1[j].x, a1.x);
+                    a1.y = fmaf(w[j], x1[j].y, a1.y);
+                    a1.z = fmaf(w[j], x1[j].z, a1.z);
+                    a1.w = fmaf(w[j], x1[j].w, a1.w);
+                }
             }
         }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(o_out + col0);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-        dst[u] = make_uint4(pack_bf16x2(acc[8 * u + 0], acc[8 * u + 1]), pack_bf16x2(acc[8 * u + 2], acc[8 * u + 3]),
-                            pack_bf16x2(acc[8 * u + 4], acc[8 * u + 5]), pack_bf16x2(acc[8 * u + 6], acc[8 * u + 7]));
+    *reinterpret_cast<uint4 *>(o_out + col0) = make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
+                                                          pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
     if (write_lse) *lse_out = L;
 }
 
-// block 128, one wave of blocks: each takes (query, 8-head group) units in turn and merges the
-// queries that were split into more than one item.  When the plan split nothing, every block
-// returns after one read of the plan header.
-__global__ void __launch_bounds__(128)
+// block kCombineThreads, one wave of blocks: each takes (query, 4-head group) units in turn and
+// merges the queries that were split into more than one item (64 threads per head row, 8
+// columns each).  When the plan split nothing, every block returns after one read of the plan
+// header.
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const PlanHeader *__restrict__ hdr, const BtInfo *__restrict__ info, const float *__restrict__ part_o,
                const float *__restrict__ part_lse, __nv_bfloat16 *__restrict__ o_lat, float *__restrict__ lse) {
     grid_launch_dependents();  // a following call's plan kernel may get resident; it waits for us
     grid_dependency_wait();    // launched as a programmatic dependent of the decode kernel
     if (hdr->n_split == 0) return;
-    const int n_units = hdr->n_bt * (kHeads / 8);
+    const int n_units = hdr->n_bt * (kHeads / kCombineHeads);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int bt = u / (kHeads / 8);
+        const int bt = u / (kHeads / kCombineHeads);
         const BtInfo in = info[bt];
         if (in.splits <= 1) continue;
-        const int h = (u % (kHeads / 8)) * 8 + (threadIdx.x >> 4);
-        const int col0 = (threadIdx.x & 15) * 32;
+        const int h = (u % (kHeads / kCombineHeads)) * kCombineHeads + (threadIdx.x >> 6);
+        const int col0 = (threadIdx.x & 63) * 8;
         combine_row(part_o + ((size_t)in.slot_base * kHeads + h) * kDc, (size_t)kHeads * kDc,
                     part_lse + (size_t)in.slot_base * kHeads + h, kHeads, in.splits, col0,
-                    o_lat + ((size_t)bt * kHeads + h) * kDc, lse + (size_t)bt * kHeads + h, (threadIdx.x & 15) == 0);
+                    o_lat + ((size_t)bt * kHeads + h) * kDc, lse + (size_t)bt * kHeads + h, (threadIdx.x & 63) == 0);
     }
 }
 
-// grid ceil(rows / 8), block 128: dense parts [n_parts, rows, 512]
-__global__ void __launch_bounds__(128)
+// grid ceil(rows / kCombineHeads), block kCombineThreads: dense parts [n_parts, rows, 512]
+__global__ void __launch_bounds__(kCombineThreads)
 combine_rows_kernel(const float *__restrict__ o_parts, const float *__restrict__ lse_parts, int n_parts, int rows,
                     __nv_bfloat16 *__restrict__ o_out, float *__restrict__ lse_out) {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 4);
+    const int row = blockIdx.x * kCombineHeads + (threadIdx.x >> 6);
     if (row >= rows) return;
-    const int col0 = (threadIdx.x & 15) * 32;
+    const int col0 = (threadIdx.x & 63) * 8;
     combine_row(o_parts + (size_t)row * kDc, (size_t)rows * kDc, lse_parts + row, (size_t)rows, n_parts, col0,
-                o_out + (size_t)row * kDc, lse_out + row, (threadIdx.x & 15) == 0);
+                o_out + (size_t)row * kDc, lse_out + row, (threadIdx.x & 63) == 0);
 }
 
 }  // namespace mla

@@ -557,9 +557,9 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
         return MLA_ERR_CUDA;
     }
     cudaLaunchConfig_t ccfg = {};
-    const int units = n_bt * (kHeads / 8);
+    const int units = n_bt * (kHeads / kCombineHeads);
     ccfg.gridDim = dim3(units < 2 * info->sms ? units : 2 * info->sms, 1, 1);
-    ccfg.blockDim = dim3(128, 1, 1);
+    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
     ccfg.stream = s;
     ccfg.attrs = &at[1];
     ccfg.numAttrs = 1;
@@ -612,7 +612,7 @@ mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_par
     DeviceInfo *info;
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
-    combine_rows_kernel<<<(rows + 7) / 8, 128, 0, (cudaStream_t)stream>>>(
+    combine_rows_kernel<<<(rows + kCombineHeads - 1) / kCombineHeads, kCombineThreads, 0, (cudaStream_t)stream>>>(
         o_parts, lse_parts, n_parts, rows, static_cast<__nv_bfloat16 *>(o_out), lse_out);
     return launch_error();
 }
