@@ -221,10 +221,17 @@ def make_append_case(name: str, seq_lens: List[int], Tq: int = 1, d_model: int =
     """A pool as make_case builds it, plus the new tokens' hidden vectors and the two weights."""
     case = make_case(name, seq_lens, Tq=Tq, causal=True, shuffle=shuffle, spare_pages=spare_pages,
                      garbage=garbage, q_mode="none", seed=seed, device=device)
-    h = _randn_bf16((len(seq_lens) * Tq, d_model), 1.0, seed, 9, device)
+    h, w_dkv, w_kr = append_inputs(len(seq_lens) * Tq, d_model, seed, device)
+    return AppendCase(case=case, h=h, w_dkv=w_dkv, w_kr=w_kr)
+
+
+def append_inputs(n_tokens: int, d_model: int = D_MODEL, seed: int = 0, device="cpu"):
+    """The cache write's inputs (tensors k = 9, 10, 11 of the recipe): h [n_tokens, d_model],
+    W^DKV [D_C, d_model], W^KR [D_R, d_model], all bf16."""
+    h = _randn_bf16((n_tokens, d_model), 1.0, seed, 9, device)
     w_dkv = _randn_bf16((D_C, d_model), 1.0 / math.sqrt(d_model), seed, 10, device)
     w_kr = _randn_bf16((D_R, d_model), 1.0 / math.sqrt(d_model), seed, 11, device)
-    return AppendCase(case=case, h=h, w_dkv=w_dkv, w_kr=w_kr)
+    return h, w_dkv, w_kr
 
 
 # Cache-write workloads: one decode step's new tokens at the decode workloads' batches, and a prefill.
