@@ -66,8 +66,14 @@ def _load():
         lib.oracle_cache_append.argtypes = [_f32p, _f32p, _f32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _f64p, _i64p]
-        for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed",
-                   "oracle_decode_naive", "oracle_combine", "oracle_rope", "oracle_cache_append"):
+        lib.oracle_compress.argtypes = [_f64p, _f64p, ctypes.c_long, ctypes.c_int, ctypes.c_int, _f64p]
+        lib.oracle_cache_append_compressed.argtypes = [_f32p, _f32p, _f32p, _f32p, _i32p, _i32p, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                       ctypes.c_double, _f64p, _i64p]
+        for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed", "oracle_decode_naive",
+                   "oracle_combine", "oracle_rope", "oracle_cache_append", "oracle_compress",
+                   "oracle_cache_append_compressed"):
             getattr(lib, fn).restype = None
         _lib = lib
     return _lib
@@ -227,4 +233,35 @@ def cache_append(h, w_dkv, w_kr, block_table, seq_lens, q_len: int, num_pages: i
         wr = np.zeros(1, dtype=np.float32)
     _load().oracle_cache_append(x, wd, wr, bt, sl, B, int(q_len), d_model, d_c, d_r, int(page), max_pages,
                                 int(num_pages), float(rope_base), rows, slot)
+    return rows, slot
+
+
+def compress(rows, z, m: int) -> np.ndarray:
+    """Merge blocks of m consecutive rows: out[g, k] = sum_i softmax_i(z[g*m+i, k]) rows[g*m+i, k]
+    (the token-level compression of the DeepSeek page's "KV cache compression" section)."""
+    r, zz = _f64(rows), _f64(z)
+    n, D = r.shape
+    assert zz.shape == r.shape and n % m == 0
+    out = np.zeros((n // m, D), dtype=np.float64)
+    _load().oracle_compress(r, zz, n // m, int(m), D, out)
+    return out
+
+
+def cache_append_compressed(h, w_dkv, w_kr, w_z, block_table, seq_lens, n_blocks: int, m: int, num_pages: int,
+                            page: int = 64, rope_base: float = 10000.0):
+    """Compressed cache write: n_blocks new compressed rows per sequence, each the merge of m new
+    tokens' rows ([W^DKV h | RoPE_pos(W^KR h)], weights softmax over the m tokens of W^Z h, per
+    component).  seq_lens counts compressed rows including the new ones.  h [B * n_blocks * m,
+    d_model].  Returns (rows [B * n_blocks, D] float64, slot [B * n_blocks] int64)."""
+    x = _f32(h)
+    wd, wr, wz = _f32(w_dkv), _f32(w_kr), _f32(w_z)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    B, max_pages = bt.shape
+    d_c, d_model = wd.shape
+    d_r = wr.shape[0]
+    x = x.reshape(B * n_blocks * m, d_model)
+    rows = np.zeros((B * n_blocks, d_c + d_r), dtype=np.float64)
+    slot = np.zeros(B * n_blocks, dtype=np.int64)
+    _load().oracle_cache_append_compressed(x, wd, wr, wz, bt, sl, B, int(n_blocks), int(m), d_model, d_c, d_r,
+                                           int(page), max_pages, int(num_pages), float(rope_base), rows, slot)
     return rows, slot

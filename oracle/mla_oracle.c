@@ -429,3 +429,94 @@ void oracle_cache_append(const float *h, const float *w_dkv, const float *w_kr, 
     }
     free(kr);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Token-level compression of the cache.                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Merge blocks of m consecutive cache rows into one row each (the DeepSeek
+ * page's "KV cache compression" section, the token-level compression of V4:
+ * the merged key-value vector is a component-wise weighted sum of the m
+ * tokens' vectors, the weights a softmax over the m tokens taken separately
+ * for every component of z = W^Z x):
+ *   out[g][k] = sum_i w[g*m+i][k] * rows[g*m+i][k],
+ *   w[g*m+i][k] = exp(z[g*m+i][k]) / sum_j exp(z[g*m+j][k]).
+ * rows, z: [n_blocks * m, D]; out: [n_blocks, D].  The softmax is taken about
+ * the block's largest z of the component (which does not change it).
+ */
+void oracle_compress(const double *rows, const double *z, long n_blocks, int m, int D, double *out) {
+    for (long g = 0; g < n_blocks; ++g) {
+        for (int k = 0; k < D; ++k) {
+            double mx = -INFINITY;
+            for (int i = 0; i < m; ++i) {
+                const double v = z[((size_t)g * m + i) * D + k];
+                if (v > mx) mx = v;
+            }
+            double den = 0.0, num = 0.0;
+            for (int i = 0; i < m; ++i) {
+                const double e = exp(z[((size_t)g * m + i) * D + k] - mx);
+                den += e;
+                num += e * rows[((size_t)g * m + i) * D + k];
+            }
+            out[(size_t)g * D + k] = num / den;
+        }
+    }
+}
+
+/*
+ * The compressed cache write: nb new compressed rows per sequence, each the
+ * merge of m new tokens.  Token rows are the cache write's (c = W^DKV h,
+ * k^R = RoPE(W^KR h) at the token's own position, row = [c | k^R]); their
+ * weights come from z = W^Z h (w_z: [d_c + d_r, d_model], row-major).
+ * seq_lens counts compressed rows and already includes the nb new ones, so
+ * the j-th new row of sequence b is compressed position P = seq_lens[b] - nb + j,
+ * merges the tokens at positions P*m .. P*m + m - 1 (h rows (b*nb + j)*m + i),
+ * and goes to pool row block_table[b, P / page] * page + P % page (slot -1 when
+ * invalid, as for the plain cache write).
+ * Outputs: rows [B*nb, D] (merged), slot [B*nb].
+ */
+void oracle_cache_append_compressed(const float *h, const float *w_dkv, const float *w_kr, const float *w_z,
+                                    const int32_t *block_table, const int32_t *seq_lens, int B, int nb, int m,
+                                    int d_model, int d_c, int d_r, int page, int max_pages, int num_pages,
+                                    double rope_base, double *rows, int64_t *slot) {
+    const int D = d_c + d_r;
+    double *tok = (double *)malloc(sizeof(double) * (size_t)m * D);
+    double *zz = (double *)malloc(sizeof(double) * (size_t)m * D);
+    double *kr = (double *)malloc(sizeof(double) * (size_t)(d_r > 0 ? d_r : 1));
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < nb; ++j) {
+            const long P = (long)seq_lens[b] - nb + j;
+            const long g = (long)b * nb + j;
+            for (int i = 0; i < m; ++i) {
+                const float *x = h + ((size_t)g * m + i) * d_model;
+                double *row = tok + (size_t)i * D;
+                for (int r = 0; r < d_c; ++r) {
+                    double acc = 0.0;
+                    for (int k = 0; k < d_model; ++k) acc += (double)w_dkv[(size_t)r * d_model + k] * (double)x[k];
+                    row[r] = acc;
+                }
+                for (int r = 0; r < d_r; ++r) {
+                    double acc = 0.0;
+                    for (int k = 0; k < d_model; ++k) acc += (double)w_kr[(size_t)r * d_model + k] * (double)x[k];
+                    kr[r] = acc;
+                }
+                oracle_rope(kr, (double)(P * m + i), d_r, rope_base, row + d_c);
+                for (int r = 0; r < D; ++r) {
+                    double acc = 0.0;
+                    for (int k = 0; k < d_model; ++k) acc += (double)w_z[(size_t)r * d_model + k] * (double)x[k];
+                    zz[(size_t)i * D + r] = acc;
+                }
+            }
+            oracle_compress(tok, zz, 1, m, D, rows + (size_t)g * D);
+            slot[g] = -1;
+            if (P >= 0 && P / page < max_pages) {
+                const int32_t pg = block_table[(size_t)b * max_pages + P / page];
+                if (pg >= 0 && pg < num_pages) slot[g] = (int64_t)pg * page + P % page;
+            }
+        }
+    }
+    free(tok);
+    free(zz);
+    free(kr);
+}

@@ -135,3 +135,17 @@ def cache_rows(h, W_dkv, W_kr, block_table, seq_lens, q_len: int, page: int, num
                 continue
             written[phys * page + offset] = _matvec(W_dkv, x) + rope_phasor(_matvec(W_kr, x), pos, base)
     return written
+
+
+def compress_block(rows, z):
+    """One merged row of a block, component by component: each token's weight is
+    1 / sum_j exp(z_j - z_i) (the softmax over the block's tokens, written as a ratio), and the
+    merged value is math.fsum of weight times value."""
+    D = len(rows[0])
+    out = []
+    for k in range(D):
+        col = [r[k] for r in rows]
+        zc = [zz[k] for zz in z]
+        w = [1.0 / math.fsum(math.exp(zj - zi) for zj in zc) for zi in zc]
+        out.append(math.fsum(wi * v for wi, v in zip(w, col)))
+    return out
