@@ -208,6 +208,33 @@ mla_status_t mla_cache_append(const void *h, const void *w_dkv, const void *w_kr
                               int max_pages, float rope_base, void *kv_pool, mla_stream_t stream);
 
 /*
+ * mla_cache_append_compressed - the cache write with token-level compression
+ * (the DeepSeek page's "KV cache compression" section: consecutive tokens are
+ * grouped in blocks of m, and each block keeps one key-value vector, the
+ * component-wise weighted sum of its tokens' vectors, with weights from a
+ * softmax over the block's tokens of each component of z = W^Z x).  Here the
+ * vector is the 576-number cache row of each token as mla_cache_append writes
+ * it (k^R turned at the token's own position), and z = W^Z h:
+ *     row[g, k] = sum_i w[i, k] * row_tok[g*m + i, k],
+ *     w[i, k]   = exp(z[g*m + i, k]) / sum_j exp(z[g*m + j, k])
+ * The merged row of block j of sequence b goes to compressed position
+ * P = seq_lens[b] - n_blocks + j (seq_lens counts compressed rows, the new ones
+ * included) and merges the tokens at positions P*m .. P*m + m - 1, h rows
+ * (b * n_blocks + j) * m + i.  mla_decode then runs on the compressed cache
+ * unchanged (each compressed row is one "token").  Only whole blocks are written.
+ *
+ * h      [batch * n_blocks * m, d_model] bf16; w_dkv [512, d_model], w_kr [64, d_model],
+ * w_z    [576, d_model] bf16 (row-major, z[k] = W^Z[k,:] . h)
+ * m      tokens per block: a power of two, 1 to 128 (1: the plain cache write)
+ * Other arguments, limits and device-side checks as mla_cache_append (positions and
+ * pages are compressed ones); batch * n_blocks * m <= 2^20.
+ */
+mla_status_t mla_cache_append_compressed(const void *h, const void *w_dkv, const void *w_kr, const void *w_z,
+                                         const int32_t *block_table, const int32_t *seq_lens, int batch,
+                                         int n_blocks, int m, int d_model, int num_pages, int max_pages,
+                                         float rope_base, void *kv_pool, mla_stream_t stream);
+
+/*
  * mla_get_device_status - synchronise `stream`, then read and clear the
  * library's device status word on the current device (MLA_DEV_* bits).
  * Returns MLA_ERR_DEVICE_FAULT if any bit was set, MLA_ERR_CUDA if the stream

@@ -66,6 +66,7 @@ EXPORTS = {
     "mla_combine": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP]),
     "mla_up_proj": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "mla_cache_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _VP]),
+    "mla_cache_append_compressed": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP]),
     "mla_get_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "mla_cache_bytes": (ctypes.c_uint64, [ctypes.c_int64, _I, _I, _I, _I]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
@@ -179,6 +180,29 @@ def cache_append(h, w_dkv, w_kr, block_table, seq_lens, kv_pool, q_len: int = 1,
                                 int(q_len), d_model, kv_pool.shape[0], block_table.shape[1], float(rope_base),
                                 _ptr(kv_pool), _stream(stream))
     _check(st, "mla_cache_append")
+    return kv_pool
+
+
+def cache_append_compressed(h, w_dkv, w_kr, w_z, block_table, seq_lens, kv_pool, n_blocks: int = 1, m: int = 4,
+                            rope_base: float = ROPE_BASE, stream=None):
+    """Compressed cache write: n_blocks new rows per sequence, each the component-wise softmax
+    merge (weights from W^Z h) of m new tokens' rows [W^DKV h | RoPE_pos(W^KR h)].
+
+    h [B * n_blocks * m, d_model] bf16, w_z [576, d_model] bf16; seq_lens counts compressed rows
+    (the new ones included).  Returns kv_pool."""
+    import torch
+    for t, n in ((h, "h"), (w_dkv, "w_dkv"), (w_kr, "w_kr"), (w_z, "w_z"), (kv_pool, "kv_pool")):
+        _need(t, torch.bfloat16, n)
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B = block_table.shape[0]
+    d_model = h.shape[-1]
+    if h.numel() != B * n_blocks * m * d_model:
+        raise ValueError(f"h: expected {B} x {n_blocks} x {m} tokens of width {d_model}")
+    st = lib().mla_cache_append_compressed(_ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(w_z), _ptr(block_table),
+                                           _ptr(seq_lens), B, int(n_blocks), int(m), d_model, kv_pool.shape[0],
+                                           block_table.shape[1], float(rope_base), _ptr(kv_pool), _stream(stream))
+    _check(st, "mla_cache_append_compressed")
     return kv_pool
 
 

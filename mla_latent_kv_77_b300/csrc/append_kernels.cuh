@@ -70,9 +70,10 @@ struct AppendParams {
     const int32_t *block_table;  // [batch, max_pages]
     const int32_t *seq_lens;     // [batch], counting the new tokens
     __nv_bfloat16 *pool;         // [num_pages, 64, 576]
-    int n_tokens, q_len, num_pages, max_pages;
+    int n_tokens, q_len, num_pages, max_pages;  // q_len: new rows per sequence (tokens, or merged blocks)
     int nkb;     // 64-wide K blocks of d_model
     int splits;  // K splits = cluster size (BN = 64 only; 1, 2, 4 or 8)
+    int m;       // compressed write: tokens merged into each row (1 for the plain write)
     int chunk;   // K blocks per copy (the tensor maps' box depth), at most the shape's kMaxChunk
     uint64_t turns[kAppendPairs];  // pair i: theta_i / (2 pi) as a fraction of 2^64
 };
@@ -157,9 +158,18 @@ struct AppendSeg {
     const CUtensorMap *map;
     int row, rows, col;
 };
-template <int BN>
+// The compressed write's column tile ct instead holds 32 row components and their 32 z
+// components: rows [32 ct, 32 ct + 32) of W^DKV or W^KR (maps a, r: 32-row boxes) in columns 0-31
+// and the same rows of W^Z (map b) in columns 32-63.
+template <int BN, bool COMP>
 __device__ __forceinline__ int append_segments(int ct, const CUtensorMap *wa, const CUtensorMap *wb,
                                                const CUtensorMap *wr, AppendSeg (&seg)[2]) {
+    if constexpr (COMP) {
+        const int c0 = ct * 32;
+        seg[0] = {c0 < kAppendLatent ? wa : wr, c0 < kAppendLatent ? c0 : c0 - kAppendLatent, 32, 0};
+        seg[1] = {wb, c0, 32, 32};
+        return 2;
+    }
     const int r0 = ct * BN, r1 = r0 + BN;
     if (r1 <= kAppendLatent) {
         seg[0] = {wa, r0, BN, 0};
@@ -174,17 +184,80 @@ __device__ __forceinline__ int append_segments(int ct, const CUtensorMap *wa, co
     return 2;
 }
 
+// The compressed write's part of the cluster reduction.  This CTA's share of the tile's rows
+// (tokens) holds whole blocks of m tokens; per block and per four components, a thread adds the
+// partners' partial sums of each token's row values (staged columns 0-31) and z values (32-63),
+// turns the k^R pairs at the token's own position, and merges the m tokens with a softmax over
+// them taken per component (running maximum, as the decode's softmax does), then writes the
+// block's four merged numbers (bf16) to the pool row of its compressed position.
+__device__ __forceinline__ void append_merge(const AppendParams &p, uint32_t base, int et, int sp, int mt, int ct,
+                                             int rows_per, int splits, bool any_abort) {
+    const int m = p.m;
+    const int blocks_here = rows_per / m;
+    for (int idx = et; idx < blocks_here * 8 && !any_abort; idx += 128) {
+        const int gl = idx >> 3, quad = idx & 7;
+        const int r_first = sp * rows_per + gl * m;
+        const int n_first = mt * kAppendTileM + r_first;
+        if (n_first >= p.n_tokens) continue;
+        int P = 0;
+        __nv_bfloat16 *dst = append_row(p, n_first / m, P);
+        const int comp = ct * 32 + quad * 4;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float den[4] = {0.f, 0.f, 0.f, 0.f}, num[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < m; ++i) {
+            const int r_in = r_first + i;
+            const uint32_t rb = base + (uint32_t)r_in * 256u;
+            const uint32_t off_v = rb + (uint32_t)((quad ^ (r_in & 7)) * 16);
+            const uint32_t off_z = off_v + 128u;
+            float4 xv[kAppendMaxSplits], xz[kAppendMaxSplits];
+#pragma unroll
+            for (int r = 0; r < kAppendMaxSplits; ++r)
+                if (r < splits) {
+                    xv[r] = ld_dsmem_f4(mapa_shared(off_v, (uint32_t)r));
+                    xz[r] = ld_dsmem_f4(mapa_shared(off_z, (uint32_t)r));
+                }
+            float4 v = xv[0], z = xz[0];
+#pragma unroll
+            for (int r = 1; r < kAppendMaxSplits; ++r)
+                if (r < splits) {
+                    v.x += xv[r].x; v.y += xv[r].y; v.z += xv[r].z; v.w += xv[r].w;
+                    z.x += xz[r].x; z.y += xz[r].y; z.z += xz[r].z; z.w += xz[r].w;
+                }
+            if (comp >= kAppendLatent) {
+                const int pair = (comp - kAppendLatent) / 2;
+                rope_pair(v.x, v.y, P * m + i, p.turns[pair]);
+                rope_pair(v.z, v.w, P * m + i, p.turns[pair + 1]);
+            }
+            const float vv[4] = {v.x, v.y, v.z, v.w}, zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float nm = fmaxf(mx[e], zz[e]);
+                const float keep = expf(mx[e] - nm), w = expf(zz[e] - nm);
+                den[e] = fmaf(den[e], keep, w);
+                num[e] = fmaf(num[e], keep, w * vv[e]);
+                mx[e] = nm;
+            }
+        }
+        if (dst != nullptr)
+            *reinterpret_cast<uint2 *>(dst + comp) = make_uint2(pack_bf16x2(num[0] / den[0], num[1] / den[1]),
+                                                                pack_bf16x2(num[2] / den[2], num[3] / den[3]));
+    }
+}
+
 // grid (splits, column tiles, token tiles), kAppendThreads threads, clusters of (splits, 1, 1).
 // Tensor maps are 3-D views (64 K, rows, K blocks) with boxes (64, rows, p.chunk):
 //   tmap_h:  h [n_tokens, d_model], AROWS-row boxes
 //   tmap_wa: W^DKV [512, d_model], BN-row boxes;  tmap_wb: W^DKV, (512 % BN)-row boxes (BN = 144)
 //   tmap_wr: W^KR [64, d_model], 64-row boxes
-template <int BN, int AROWS>
+// COMP (the compressed write, BN = 64 only): tmap_wa, tmap_wr with 32-row boxes, and tmap_wb is
+// W^Z [576, d_model] with 32-row boxes.
+template <int BN, int AROWS, bool COMP>
 __global__ void __launch_bounds__(kAppendThreads, 1)
 append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_wa,
               const __grid_constant__ CUtensorMap tmap_wb, const __grid_constant__ CUtensorMap tmap_wr,
               const __grid_constant__ AppendParams p) {
     using S = AppendShape<BN, AROWS>;
+    static_assert(!COMP || S::kReduce, "the compressed write merges rows in the cluster reduction");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -205,7 +278,7 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
     volatile int *abort = reinterpret_cast<volatile int *>(smem_raw + (base - raw) + S::kRegionCap + 248);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + (base - raw) + S::kRegionCap + 240);
     AppendSeg seg[2];
-    const int n_seg = append_segments<BN>(ct, &tmap_wa, &tmap_wb, &tmap_wr, seg);
+    const int n_seg = append_segments<BN, COMP>(ct, &tmap_wa, &tmap_wb, &tmap_wr, seg);
     Tracer tr;
     tr.at(0x8101);
 
@@ -312,7 +385,7 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        if constexpr (S::kReduce) {
+        if constexpr (S::kReduce && !COMP) {
             if (et < rows_per * kChunks4) {
                 const int n = mt * kAppendTileM + sp * rows_per + et / kChunks4;
                 if (n < p.n_tokens) pre_dst = append_row(p, n, pre_pos);
@@ -379,6 +452,9 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
             const int splits = p.splits;
             bool any_abort = false;
             for (int r = 0; r < splits; ++r) any_abort |= ld_dsmem_u32(mapa_shared(abort_addr, (uint32_t)r)) != 0u;
+            if constexpr (COMP) {
+                append_merge(p, base, et, sp, mt, ct, rows_per, splits, any_abort);
+            } else
             // this CTA's rows of the tile: rows_per = AROWS / splits rows of BN / 4 four-column chunks
             for (int idx = et; idx < rows_per * kChunks4 && !any_abort; idx += 128) {
                 const int r_in = sp * rows_per + idx / kChunks4, chunk = idx % kChunks4;

@@ -60,8 +60,9 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
             // SMs need not switch their L1 / shared split between the plan, decode and combine
             for (const void *fn : {(const void *)plan_kernel, (const void *)combine_kernel,
                                    (const void *)combine_rows_kernel, (const void *)decode_kernel,
-                                   (const void *)head_gemm_kernel, (const void *)append_kernel<64, 64>,
-                                   (const void *)append_kernel<64, 128>, (const void *)append_kernel<144, 128>})
+                                   (const void *)head_gemm_kernel, (const void *)append_kernel<64, 64, false>,
+                                   (const void *)append_kernel<64, 128, false>, (const void *)append_kernel<144, 128, false>,
+                                   (const void *)append_kernel<64, 64, true>, (const void *)append_kernel<64, 128, true>})
                 cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
             cudaGetLastError();
@@ -69,12 +70,16 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
                     cudaSuccess ||
                 cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemMax) !=
                     cudaSuccess ||
-                cudaFuncSetAttribute(append_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(append_kernel<64, 64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)AppendShape<64, 64>::kSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(append_kernel<64, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(append_kernel<64, 128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)AppendShape<64, 128>::kSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(append_kernel<144, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)AppendShape<144, 128>::kSmem) != cudaSuccess)
+                cudaFuncSetAttribute(append_kernel<144, 128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<144, 128>::kSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(append_kernel<64, 64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<64, 64>::kSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(append_kernel<64, 128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AppendShape<64, 128>::kSmem) != cudaSuccess)
                 return MLA_ERR_CUDA;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
@@ -358,6 +363,7 @@ mla_status_t mla_cache_append(const void *h, const void *w_dkv, const void *w_kr
     p.nkb = d_model / 64;
     p.splits = cf.splits;
     p.chunk = cf.chunk;
+    p.m = 1;
     for (int i = 0; i < kAppendPairs; ++i) p.turns[i] = rope_turns((double)rope_base, i);
     const unsigned token_tiles = (unsigned)((n_tokens + kAppendTileM - 1) / kAppendTileM);
     cudaLaunchConfig_t cfg = {};
@@ -374,16 +380,87 @@ mla_status_t mla_cache_append(const void *h, const void *w_dkv, const void *w_kr
     if (cf.bn == 64 && cf.arows == 64) {
         cfg.gridDim = dim3((unsigned)cf.splits, AppendShape<64, 64>::kColTiles, token_tiles);
         cfg.dynamicSmemBytes = AppendShape<64, 64>::kSmem;
-        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 64>, th, twa, twb, twr, p);
+        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 64, false>, th, twa, twb, twr, p);
     } else if (cf.bn == 64) {
         cfg.gridDim = dim3((unsigned)cf.splits, AppendShape<64, 128>::kColTiles, token_tiles);
         cfg.dynamicSmemBytes = AppendShape<64, 128>::kSmem;
-        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 128>, th, twa, twb, twr, p);
+        e = cudaLaunchKernelEx(&cfg, append_kernel<64, 128, false>, th, twa, twb, twr, p);
     } else {
         cfg.gridDim = dim3(1, AppendShape<144, 128>::kColTiles, token_tiles);
         cfg.dynamicSmemBytes = AppendShape<144, 128>::kSmem;
-        e = cudaLaunchKernelEx(&cfg, append_kernel<144, 128>, th, twa, twb, twr, p);
+        e = cudaLaunchKernelEx(&cfg, append_kernel<144, 128, false>, th, twa, twb, twr, p);
     }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    return launch_error(1);
+}
+
+mla_status_t mla_cache_append_compressed(const void *h, const void *w_dkv, const void *w_kr, const void *w_z,
+                                         const int32_t *block_table, const int32_t *seq_lens, int batch, int n_blocks,
+                                         int m, int d_model, int num_pages, int max_pages, float rope_base,
+                                         void *kv_pool, mla_stream_t stream) {
+    if (!h || !w_dkv || !w_kr || !w_z || !block_table || !seq_lens || !kv_pool) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || n_blocks < 1 || num_pages < 1 || max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (m < 1 || m > kAppendTileM || (m & (m - 1)) != 0) return MLA_ERR_INVALID_ARG;
+    if (!(rope_base > 1.f) || !std::isfinite(rope_base)) return MLA_ERR_INVALID_ARG;
+    const long long n_tokens = (long long)batch * n_blocks * m;
+    if (n_tokens > kMaxAppendTokens || d_model < 64 || d_model % 64 != 0 || d_model > kMaxDModel) return MLA_ERR_SHAPE;
+    if ((long long)num_pages * kPage > 0x7fffffffll || (long long)max_pages * kPage > 0x7fffffffll) return MLA_ERR_SHAPE;
+    if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(w_z) || !aligned16(kv_pool) ||
+        !aligned4(block_table) || !aligned4(seq_lens))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    // 64-column tiles of 32 row components and their 32 z components; K split over a cluster of
+    // at most 4 CTAs (so the 18 column tiles' clusters all fit at once), and at most as many as
+    // leave each CTA whole blocks of m tokens in the reduction
+    const int tiles = (int)((n_tokens + kAppendTileM - 1) / kAppendTileM);
+    const int nkb = d_model / 64;
+    const int arows = n_tokens <= 64 ? 64 : 128;
+    int sp = 1;
+    while (2 * sp <= 4 && 2 * sp * tiles <= kAppendMaxSplits && 2 * sp <= nkb && arows / (2 * sp) >= m) sp *= 2;
+    const int nk_max = (nkb + sp - 1) / sp;
+    const int cap = arows == 64 ? AppendShape<64, 64>::kMaxChunk : AppendShape<64, 128>::kMaxChunk;
+    int chunk = (nk_max + 4) / 5;
+    if (chunk > cap) chunk = cap;
+    if (chunk < 1) chunk = 1;
+    CUtensorMap th, twa, twz, twr;
+    if (!tmap_col_blocks(&th, h, (uint64_t)n_tokens, (uint32_t)nkb, (uint32_t)arows, (uint32_t)chunk) ||
+        !tmap_col_blocks(&twa, w_dkv, kAppendLatent, (uint32_t)nkb, 32, (uint32_t)chunk) ||
+        !tmap_col_blocks(&twr, w_kr, kAppendCols - kAppendLatent, (uint32_t)nkb, 32, (uint32_t)chunk) ||
+        !tmap_col_blocks(&twz, w_z, kAppendCols, (uint32_t)nkb, 32, (uint32_t)chunk))
+        return MLA_ERR_CUDA;
+    AppendParams p;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.pool = static_cast<__nv_bfloat16 *>(kv_pool);
+    p.n_tokens = (int)n_tokens;
+    p.q_len = n_blocks;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.nkb = nkb;
+    p.splits = sp;
+    p.chunk = chunk;
+    p.m = m;
+    for (int i = 0; i < kAppendPairs; ++i) p.turns[i] = rope_turns((double)rope_base, i);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kAppendThreads, 1, 1);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)sp;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)sp, kAppendCols / 32, (unsigned)tiles);
+    cfg.dynamicSmemBytes = AppendShape<64, 64>::kSmem;
+    cudaError_t e = arows == 64 ? cudaLaunchKernelEx(&cfg, append_kernel<64, 64, true>, th, twa, twz, twr, p)
+                                : cudaLaunchKernelEx(&cfg, append_kernel<64, 128, true>, th, twa, twz, twr, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;

@@ -155,6 +155,22 @@ def test_cache_append_rejects_bad_arguments_on_host(lib, over, code):
     assert _call_append(lib, _append_args(**over)) == code
 
 
+def test_cache_append_compressed_rejects_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+
+    def call(m=4, nb=1, d=5120, wz=64, pool=96):
+        return lib.mla_cache_append_compressed(vp(16), vp(32), vp(48), vp(wz) if wz else None, vp(80), vp(112), 2, nb,
+                                               m, d, 4, 2, 10000.0, vp(pool), None)
+    assert call(wz=None) == mla.Status.INVALID_ARG
+    assert call(m=3) == mla.Status.INVALID_ARG
+    assert call(m=256) == mla.Status.INVALID_ARG
+    assert call(m=0) == mla.Status.INVALID_ARG
+    assert call(nb=0) == mla.Status.INVALID_ARG
+    assert call(d=100) == mla.Status.SHAPE
+    assert call(wz=72) == mla.Status.ALIGNMENT
+    assert call(pool=104) == mla.Status.ALIGNMENT
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mla, "_lib", None)
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
