@@ -379,7 +379,8 @@ def fused_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
 def append_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict:
     """The cache write (mla_cache_append: c = W^DKV h, rotated k^R, scattered into the pool) on its
     three workloads: one decode step's 64 new tokens, the causal step's 128, and a 4096-token
-    prompt, all at d_model 5120.  Captured into a CUDA graph and replayed (graph_us); inputs larger
+    prompt, all at d_model 5120; and the compressed write (mla_cache_append_compressed) with
+    blocks of 4 (64 tokens) and of 128.  Captured into a CUDA graph and replayed (graph_us); inputs larger
     than L2: the calls cycle through copies of (h, W^DKV, W^KR) covering twice the 126 MB L2.
     Roofline: the HBM bytes a call must move (both weights, h, the written rows) and the tensor
     FLOPs (2 x tokens x 576 x d_model); the prompt is the tensor-bound one."""
@@ -414,6 +415,33 @@ def append_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict
                      "tflops": tf, "frac_tensor": tf / pk["bf16_tflops"], "t_roof_us": t_roof * 1e6,
                      "roofline_frac": t_roof / (us * 1e-6), "launches_per_call": launches, "copies": copies}
         del hs, wds, wrs, ac, c, pool
+        torch.cuda.empty_cache()
+    for name in workloads.COMPRESS_WORKLOADS:
+        cc = workloads.make_compress_workload(name, seed=0, device=dev)
+        c = cc.case
+        n, d = cc.n_tokens, cc.d_model
+        copies = _l2_copies(cc.weight_bytes() + n * d * 2)
+        hs = [cc.h.clone() for _ in range(copies)]
+        wds = [cc.w_dkv.clone() for _ in range(copies)]
+        wrs = [cc.w_kr.clone() for _ in range(copies)]
+        wzs = [cc.w_z.clone() for _ in range(copies)]
+        bt, sl, pool = c.block_table.to(dev), c.seq_lens.to(dev), c.pool
+
+        def ccall(k):
+            return lambda st: mla.cache_append_compressed(hs[k], wds[k], wrs[k], wzs[k], bt, sl, pool,
+                                                          n_blocks=cc.n_blocks, m=cc.m, stream=st)
+        for i in range(max(warmup, copies)):
+            ccall(i % copies)(stream)
+        torch.cuda.synchronize()
+        us = graph_us([ccall(k) for k in range(copies)], max(1, steps // copies))
+        bytes_ = cc.weight_bytes() + n * d * 2 + (n // cc.m) * ROW_BYTES
+        flops = 2.0 * n * 2 * 576 * d
+        gbs = bytes_ / (us * 1e-6) / 1e9
+        t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+        res[name] = {"tokens": n, "m": cc.m, "us": us, "bytes": bytes_, "achieved_gbs": gbs,
+                     "frac_hbm": gbs / pk["hbm_gbs"], "t_roof_us": t_roof * 1e6,
+                     "roofline_frac": t_roof / (us * 1e-6), "copies": copies}
+        del hs, wds, wrs, wzs, cc, c, pool
         torch.cuda.empty_cache()
     st, word = mla.get_device_status()
     assert st == 0, f"device status {word:#x}"

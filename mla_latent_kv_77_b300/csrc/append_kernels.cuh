@@ -184,19 +184,69 @@ __device__ __forceinline__ int append_segments(int ct, const CUtensorMap *wa, co
     return 2;
 }
 
-// The compressed write's part of the cluster reduction.  This CTA's share of the tile's rows
-// (tokens) holds whole blocks of m tokens; per block and per four components, a thread adds the
-// partners' partial sums of each token's row values (staged columns 0-31) and z values (32-63),
-// turns the k^R pairs at the token's own position, and merges the m tokens with a softmax over
-// them taken per component (running maximum, as the decode's softmax does), then writes the
-// block's four merged numbers (bf16) to the pool row of its compressed position.
+// The compressed write's part of the cluster reduction.  The CTAs of the cluster share the
+// tile's 32 components (8 four-component groups, 8 / splits each), all rows: per block of m
+// tokens and per four components, a thread adds the partners' partial sums of each token's row
+// values (staged columns 0-31) and z values (32-63), turns the k^R pairs at the token's own
+// position, and merges the m tokens with a softmax over them taken per component (running
+// maximum, as the decode's softmax does), then writes the block's four merged numbers (bf16) to
+// the pool row of its compressed position.
+// One token's contribution to a block's merge, for four components: the partners' partial sums
+// of its row values and z values, its k^R pairs turned at its position, then the running
+// softmax update (max, denominator, numerator) per component.
+__device__ __forceinline__ void append_merge_token(const AppendParams &p, uint32_t base, int r_in, int quad, int comp,
+                                                   int pos, int splits, float (&mx)[4], float (&den)[4],
+                                                   float (&num)[4]) {
+    const uint32_t off_v = base + (uint32_t)r_in * 256u + (uint32_t)((quad ^ (r_in & 7)) * 16);
+    const uint32_t off_z = off_v + 128u;
+    float4 xv[kAppendMaxSplits], xz[kAppendMaxSplits];
+#pragma unroll
+    for (int r = 0; r < kAppendMaxSplits; ++r)
+        if (r < splits) {
+            xv[r] = ld_dsmem_f4(mapa_shared(off_v, (uint32_t)r));
+            xz[r] = ld_dsmem_f4(mapa_shared(off_z, (uint32_t)r));
+        }
+    float4 v = xv[0], z = xz[0];
+#pragma unroll
+    for (int r = 1; r < kAppendMaxSplits; ++r)
+        if (r < splits) {
+            v.x += xv[r].x; v.y += xv[r].y; v.z += xv[r].z; v.w += xv[r].w;
+            z.x += xz[r].x; z.y += xz[r].y; z.z += xz[r].z; z.w += xz[r].w;
+        }
+    if (comp >= kAppendLatent) {
+        const int pair = (comp - kAppendLatent) / 2;
+        rope_pair(v.x, v.y, pos, p.turns[pair]);
+        rope_pair(v.z, v.w, pos, p.turns[pair + 1]);
+    }
+    const float vv[4] = {v.x, v.y, v.z, v.w}, zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float nm = fmaxf(mx[e], zz[e]);
+        const float keep = expf(mx[e] - nm), w = expf(zz[e] - nm);
+        den[e] = fmaf(den[e], keep, w);
+        num[e] = fmaf(num[e], keep, w * vv[e]);
+        mx[e] = nm;
+    }
+}
+
+// The compressed write's part of the cluster reduction.  The CTAs of the cluster share the
+// tile's 32 components (8 four-component groups, 8 / splits each), all rows: per block of m
+// tokens and per four components the partners' partial sums of each token's row values (staged
+// columns 0-31) and z values (32-63) are added, the k^R pairs turned at the token's own position,
+// and the m tokens merged with a softmax over them taken per component (running maximum, as the
+// decode's softmax does); the block's four merged numbers go (bf16) to the pool row of its
+// compressed position.  Blocks of fewer than 32 tokens take one thread each; larger ones a warp,
+// whose lanes take every 32nd token and then combine their running sums.
+template <int AROWS>
 __device__ __forceinline__ void append_merge(const AppendParams &p, uint32_t base, int et, int sp, int mt, int ct,
-                                             int rows_per, int splits, bool any_abort) {
+                                             int splits, bool any_abort) {
     const int m = p.m;
-    const int blocks_here = rows_per / m;
-    for (int idx = et; idx < blocks_here * 8 && !any_abort; idx += 128) {
-        const int gl = idx >> 3, quad = idx & 7;
-        const int r_first = sp * rows_per + gl * m;
+    const int blocks = AROWS / m, quads = 8 / splits;
+    const bool by_warp = m >= 32;
+    const int lane = et & 31, workers = by_warp ? 4 : 128, me = by_warp ? et >> 5 : et;
+    for (int idx = me; idx < blocks * quads && !any_abort; idx += workers) {
+        const int gl = idx / quads, quad = sp * quads + idx % quads;
+        const int r_first = gl * m;
         const int n_first = mt * kAppendTileM + r_first;
         if (n_first >= p.n_tokens) continue;
         int P = 0;
@@ -204,39 +254,25 @@ __device__ __forceinline__ void append_merge(const AppendParams &p, uint32_t bas
         const int comp = ct * 32 + quad * 4;
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float den[4] = {0.f, 0.f, 0.f, 0.f}, num[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = 0; i < m; ++i) {
-            const int r_in = r_first + i;
-            const uint32_t rb = base + (uint32_t)r_in * 256u;
-            const uint32_t off_v = rb + (uint32_t)((quad ^ (r_in & 7)) * 16);
-            const uint32_t off_z = off_v + 128u;
-            float4 xv[kAppendMaxSplits], xz[kAppendMaxSplits];
+        if (by_warp) {
+            for (int i = lane; i < m; i += 32) append_merge_token(p, base, r_first + i, quad, comp, P * m + i, splits, mx, den, num);
 #pragma unroll
-            for (int r = 0; r < kAppendMaxSplits; ++r)
-                if (r < splits) {
-                    xv[r] = ld_dsmem_f4(mapa_shared(off_v, (uint32_t)r));
-                    xz[r] = ld_dsmem_f4(mapa_shared(off_z, (uint32_t)r));
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, mx[e], o);
+                    const float d2 = __shfl_xor_sync(0xffffffffu, den[e], o);
+                    const float n2 = __shfl_xor_sync(0xffffffffu, num[e], o);
+                    const float nm = fmaxf(mx[e], m2);
+                    const float a = expf(mx[e] - nm), b = expf(m2 - nm);
+                    den[e] = den[e] * a + d2 * b;
+                    num[e] = num[e] * a + n2 * b;
+                    mx[e] = nm;
                 }
-            float4 v = xv[0], z = xz[0];
-#pragma unroll
-            for (int r = 1; r < kAppendMaxSplits; ++r)
-                if (r < splits) {
-                    v.x += xv[r].x; v.y += xv[r].y; v.z += xv[r].z; v.w += xv[r].w;
-                    z.x += xz[r].x; z.y += xz[r].y; z.z += xz[r].z; z.w += xz[r].w;
-                }
-            if (comp >= kAppendLatent) {
-                const int pair = (comp - kAppendLatent) / 2;
-                rope_pair(v.x, v.y, P * m + i, p.turns[pair]);
-                rope_pair(v.z, v.w, P * m + i, p.turns[pair + 1]);
             }
-            const float vv[4] = {v.x, v.y, v.z, v.w}, zz[4] = {z.x, z.y, z.z, z.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float nm = fmaxf(mx[e], zz[e]);
-                const float keep = expf(mx[e] - nm), w = expf(zz[e] - nm);
-                den[e] = fmaf(den[e], keep, w);
-                num[e] = fmaf(num[e], keep, w * vv[e]);
-                mx[e] = nm;
-            }
+            if (lane != 0) continue;
+        } else {
+            for (int i = 0; i < m; ++i) append_merge_token(p, base, r_first + i, quad, comp, P * m + i, splits, mx, den, num);
         }
         if (dst != nullptr)
             *reinterpret_cast<uint2 *>(dst + comp) = make_uint2(pack_bf16x2(num[0] / den[0], num[1] / den[1]),
@@ -453,7 +489,7 @@ append_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant_
             bool any_abort = false;
             for (int r = 0; r < splits; ++r) any_abort |= ld_dsmem_u32(mapa_shared(abort_addr, (uint32_t)r)) != 0u;
             if constexpr (COMP) {
-                append_merge(p, base, et, sp, mt, ct, rows_per, splits, any_abort);
+                append_merge<AROWS>(p, base, et, sp, mt, ct, splits, any_abort);
             } else
             // this CTA's rows of the tile: rows_per = AROWS / splits rows of BN / 4 four-column chunks
             for (int idx = et; idx < rows_per * kChunks4 && !any_abort; idx += 128) {

@@ -416,13 +416,13 @@ mla_status_t mla_cache_append_compressed(const void *h, const void *w_dkv, const
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
     // 64-column tiles of 32 row components and their 32 z components; K split over a cluster of
-    // at most 4 CTAs (so the 18 column tiles' clusters all fit at once), and at most as many as
-    // leave each CTA whole blocks of m tokens in the reduction
+    // at most 4 CTAs (so the 18 column tiles' clusters all fit at once), which share the merge by
+    // components
     const int tiles = (int)((n_tokens + kAppendTileM - 1) / kAppendTileM);
     const int nkb = d_model / 64;
     const int arows = n_tokens <= 64 ? 64 : 128;
     int sp = 1;
-    while (2 * sp <= 4 && 2 * sp * tiles <= kAppendMaxSplits && 2 * sp <= nkb && arows / (2 * sp) >= m) sp *= 2;
+    while (2 * sp <= 4 && 2 * sp * tiles <= kAppendMaxSplits && 2 * sp <= nkb) sp *= 2;
     const int nk_max = (nkb + sp - 1) / sp;
     const int cap = arows == 64 ? AppendShape<64, 64>::kMaxChunk : AppendShape<64, 128>::kMaxChunk;
     int chunk = (nk_max + 4) / 5;

@@ -22,6 +22,7 @@ reproducible on its own; the ragged lengths come first, from a generator seeded
   k=9  h (cache write: the new tokens' hidden vectors) ~ N(0, 1), bf16
   k=10 W^DKV        ~ N(0, 1) / sqrt(d_model), bf16   (so c ~ N(0, 1))
   k=11 W^KR         ~ N(0, 1) / sqrt(d_model), bf16
+  k=12 W^Z (compressed cache write) ~ N(0, 1) / sqrt(d_model), bf16
 
 Shapes follow the DeepSeek-V2 attention: 128 heads, 512-d latent, 64-d decoupled
 RoPE key, 128-d head, 576-number cache row, 64-token pages.
@@ -247,3 +248,49 @@ APPEND_WORKLOADS = {
 
 def make_append_workload(name: str, seed: int = 0, device="cpu") -> AppendCase:
     return make_append_case(name, seed=seed, device=device, **APPEND_WORKLOADS[name])
+
+
+@dataclass
+class CompressCase:
+    """A compressed cache write: n_blocks new rows per sequence, each merging m new tokens."""
+    case: Case                      # the pool, block table, compressed lengths
+    h: torch.Tensor                 # [B * n_blocks * m, d_model] bf16
+    w_dkv: torch.Tensor
+    w_kr: torch.Tensor
+    w_z: torch.Tensor               # [D, d_model] bf16
+    n_blocks: int
+    m: int
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.h.shape[0])
+
+    @property
+    def d_model(self) -> int:
+        return int(self.h.shape[1])
+
+    def weight_bytes(self) -> int:
+        return 2 * D * self.d_model * 2
+
+
+def make_compress_case(name: str, seq_lens: List[int], n_blocks: int, m: int, d_model: int = D_MODEL,
+                       shuffle: bool = False, seed: int = 0, device="cpu") -> CompressCase:
+    """seq_lens: compressed lengths, the n_blocks new rows included."""
+    case = make_case(name, seq_lens, Tq=n_blocks, causal=True, shuffle=shuffle, q_mode="none", seed=seed,
+                     device=device)
+    h, w_dkv, w_kr = append_inputs(len(seq_lens) * n_blocks * m, d_model, seed, device)
+    w_z = _randn_bf16((D, d_model), 1.0 / math.sqrt(d_model), seed, 12, device)
+    return CompressCase(case=case, h=h, w_dkv=w_dkv, w_kr=w_kr, w_z=w_z, n_blocks=n_blocks, m=m)
+
+
+# Compressed cache-write workloads: CSA's blocks of 4 and HCA's blocks of 128 (m from the page).
+COMPRESS_WORKLOADS = {
+    # 16 sequences, one new block of 4 tokens each (64 tokens), after 1023 compressed rows
+    "compress_b16_m4": dict(seq_lens=[1024] * 16, n_blocks=1, m=4),
+    # one sequence, one new block of 128 tokens, after 31 compressed rows
+    "compress_b1_m128": dict(seq_lens=[32], n_blocks=1, m=128),
+}
+
+
+def make_compress_workload(name: str, seed: int = 0, device="cpu") -> CompressCase:
+    return make_compress_case(name, seed=seed, device=device, **COMPRESS_WORKLOADS[name])
