@@ -448,6 +448,60 @@ def append_leg(mla, workloads, dev, stream, steps: int, warmup: int, pk) -> dict
     return res
 
 
+def other_workloads_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_index: int = 0) -> dict:
+    """The decode on the other large workloads, timed as the headline is (K calls back to back
+    between one event pair, two alternating caches so no call finds its cache in L2): the
+    batch-8 131072-token peaked rows, the 128 ragged sequences on a randomly paged pool, and
+    the batch-32 four-query causal decode.  Per workload: us per call, tokens/s, and the
+    fraction of the roofline (HBM bytes or bf16 FLOPs, whichever binds)."""
+    import torch
+    res = {"unit": "us per call", "steps": steps,
+           "timing": "K calls back to back between one event pair; two alternating caches"}
+    stream = torch.cuda.current_stream()
+    for name in ("b32_tq4_causal_fused", "b8_l128k_peaked", "b128_ragged32k"):
+        case = workloads.make_workload(name, seed=0, device=dev)
+        pools = [case.pool, case.pool.clone()]
+        q_abs = case.q_abs if case.q_abs is not None else mla.absorb_q(case.q_nope, case.q_rope, case.w_uk)
+        q_abs = q_abs.view(case.B, case.Tq, 128, 576)
+        bt, sl = case.block_table.to(dev), case.seq_lens.to(dev)
+        o = torch.empty(case.B, case.Tq, 128, 512, dtype=torch.bfloat16, device=dev)
+        l = torch.empty(case.B, case.Tq, 128, dtype=torch.float32, device=dev)
+        ws = torch.empty(mla.decode_workspace_size(case.B, case.Tq, 0), dtype=torch.uint8, device=dev)
+
+        def call(i):
+            mla.decode(q_abs, pools[i & 1], bt, sl, case.scale, causal=case.causal, o_lat=o, lse=l, workspace=ws,
+                       stream=stream)
+        for i in range(warmup):
+            call(i)
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_index) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            clk.mark_begin()
+            e0.record(stream)
+            for i in range(steps):
+                call(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            clk.mark_end()
+        us = e0.elapsed_time(e1) * 1000.0 / steps
+        lens = case.seq_lens.to(torch.int64)
+        cache = int(lens.sum()) * ROW_BYTES
+        if case.causal:
+            vis = sum(max(0, int(L) - (case.Tq - 1 - t)) for L in case.seq_lens for t in range(case.Tq))
+        else:
+            vis = int(lens.sum()) * case.Tq
+        flops = vis * FLOP_PER_TOKEN_QUERY
+        t_mem, t_tc = cache / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12)
+        res[name] = {"us": us, "tokens_per_s": case.B * case.Tq / (us * 1e-6), "cache_bytes": cache,
+                     "bound": "hbm" if t_mem >= t_tc else "tensor",
+                     "roofline_frac": max(t_mem, t_tc) / (us * 1e-6), "clocks": clk.summary()}
+        st, word = mla.get_device_status()
+        assert st == 0, f"device status {word:#x}"
+        del case, pools, q_abs, o, l, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each step
     decodes a bounded sample (`--ref-seqs` whole sequences, all heads and query tokens) of
@@ -501,6 +555,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused absorb/decode/up-projection timing")
     ap.add_argument("--no-append", action="store_true", help="skip the cache-write timing")
+    ap.add_argument("--no-others", action="store_true", help="skip the other large workloads' decode timing")
     ap.add_argument("--ref-seqs", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -641,6 +696,10 @@ def main():
     fused = None
     if rank == 0 and args.workload == "b64_l4096" and not args.no_fused:
         fused = fused_leg(mla, workloads, dev, stream, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks())
+    others = None
+    if rank == 0 and world == 1 and args.workload == "b64_l4096" and not args.no_others:
+        others = other_workloads_leg(mla, workloads, dev, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks(),
+                                     gpu_index=local)
     append = None
     if rank == 0 and args.workload == "b64_l4096" and not args.no_append:
         append = append_leg(mla, workloads, dev, stream, steps=max(args.steps, 20), warmup=args.warmup, pk=peaks())
@@ -680,6 +739,7 @@ def main():
             "cpu_baseline": cpu,
             "fused": fused,
             "append": append,
+            "other_workloads": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
