@@ -13,7 +13,10 @@ Sources (see the C file for the passage each function follows):
     RoPE, 576-number cache row; the cache write c = W^DKV h of equation 9 and
     the rotated key k^R of Step 7);
   * DeepSeek-V2 paper breakdown, "How It Works" (latent c_t cached, up-projected
-    to K and V, separate RoPE key kept beside it).
+    to K and V, separate RoPE key kept beside it);
+  * the DeepSeek page, "KV cache compression" (token-level compression) and
+    "KV cache data movement minimization" (the indexer: index scores over every
+    cached token, top-k, attention over the selected tokens only).
 """
 from __future__ import annotations
 
@@ -71,9 +74,14 @@ def _load():
                                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                        ctypes.c_double, _f64p, _i64p]
+        lib.oracle_index_scores.argtypes = [_f32p, _f32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_long, _f64p]
+        lib.oracle_topk_row.argtypes = [_f64p, ctypes.c_long, ctypes.c_long,
+                                        np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")]
+        lib.oracle_topk_row.restype = ctypes.c_long
         for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed", "oracle_decode_naive",
                    "oracle_combine", "oracle_rope", "oracle_cache_append", "oracle_compress",
-                   "oracle_cache_append_compressed"):
+                   "oracle_cache_append_compressed", "oracle_index_scores"):
             getattr(lib, fn).restype = None
         _lib = lib
     return _lib
@@ -265,3 +273,52 @@ def cache_append_compressed(h, w_dkv, w_kr, w_z, block_table, seq_lens, n_blocks
     _load().oracle_cache_append_compressed(x, wd, wr, wz, bt, sl, B, int(n_blocks), int(m), d_model, d_c, d_r,
                                            int(page), max_pages, int(num_pages), float(rope_base), rows, slot)
     return rows, slot
+
+
+def index_scores(q_idx, idx_pool, block_table, seq_lens, max_len: int | None = None) -> np.ndarray:
+    """s[b, t] = q_idx[b] . k_idx(b, t) for t < seq_lens[b] (NaN elsewhere): the indexer's
+    scores over every cached token (the DeepSeek page's "indexer" method).  q_idx [B, d_idx],
+    idx_pool [P, page, d_idx]."""
+    q, ip = _f32(q_idx), _f32(idx_pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    B, d_idx = q.shape
+    page = ip.shape[1]
+    if max_len is None:
+        max_len = int(sl.max()) if sl.size else 0
+    out = np.full((B, max(1, max_len)), np.nan, dtype=np.float64)
+    _load().oracle_index_scores(q, ip, bt, sl, B, d_idx, page, bt.shape[1], max(1, max_len), out)
+    return out[:, :max_len]
+
+
+def topk_row(scores, k: int) -> np.ndarray:
+    """Indices of the k largest scores (ties: the lower index), ascending; all if k >= n."""
+    s = _f64(scores).reshape(-1)
+    out = np.zeros(max(1, min(k, s.size)), dtype=np.int64)
+    n = _load().oracle_topk_row(s, s.size, int(k), out)
+    return out[:n]
+
+
+def decode_sparse(q_abs, q_idx, pool, idx_pool, block_table, seq_lens, k: int, scale: float, d_c: int = 512):
+    """Top-k sparse decode (one query token per sequence): index scores over every cached token,
+    the k best (ties: lower index), then the absorbed decode over those tokens only.
+    Returns (o_lat [B, 1, H, d_c], lse [B, 1, H], selected: list of index arrays)."""
+    q = _f64(q_abs)
+    B = q.shape[0]
+    pl = _f32(pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    page, D = pl.shape[1], pl.shape[2]
+    sc = index_scores(q_idx, idx_pool, bt, sl)
+    sel, rows = [], []
+    for b in range(B):
+        idx = topk_row(sc[b, :int(sl[b])], k) if sl[b] > 0 else np.zeros(0, dtype=np.int64)
+        sel.append(idx)
+        rows.append(np.stack([pl[bt[b, t // page], t % page] for t in idx]) if idx.size else np.zeros((0, D), np.float32))
+    kmax = max(1, max(r.shape[0] for r in rows))
+    n_pages = (kmax + page - 1) // page
+    comp = np.zeros((B * n_pages, page, D), dtype=np.float32)
+    cbt = np.arange(B * n_pages, dtype=np.int32).reshape(B, n_pages)
+    lens = np.array([r.shape[0] for r in rows], dtype=np.int32)
+    for b in range(B):
+        comp.reshape(B, n_pages * page, D)[b, :rows[b].shape[0]] = rows[b]
+    o, lse = decode_absorbed(q, comp, cbt, lens, scale, causal=False, d_c=d_c)
+    return o, lse, sel

@@ -520,3 +520,61 @@ void oracle_cache_append_compressed(const float *h, const float *w_dkv, const fl
     free(zz);
     free(kr);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Indexer: top-k sparse decode.                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Index scores (the DeepSeek page's "KV cache data movement minimization"
+ * section: every cached vector also has a small index vector; a decoding
+ * token scores all of them, keeps the top k, and attends over those tokens
+ * only).  s[b][t] = q_idx[b] . k_idx(b, t) for t < seq_lens[b], where
+ * k_idx(b, t) = idx_pool[block_table[b, t / page], t % page, :] (d_idx wide);
+ * entries t >= seq_lens[b] are left untouched.  scores: [B, max_len].
+ */
+void oracle_index_scores(const float *q_idx, const float *idx_pool, const int32_t *block_table,
+                         const int32_t *seq_lens, int B, int d_idx, int page, int max_pages, long max_len,
+                         double *scores) {
+    for (int b = 0; b < B; ++b) {
+        const long L = seq_lens[b];
+        for (long t = 0; t < L && t < max_len; ++t) {
+            const float *k = idx_pool + ((size_t)block_table[(size_t)b * max_pages + t / page] * page + t % page) * d_idx;
+            double acc = 0.0;
+            for (int d = 0; d < d_idx; ++d) acc += (double)q_idx[(size_t)b * d_idx + d] * (double)k[d];
+            scores[(size_t)b * max_len + t] = acc;
+        }
+    }
+}
+
+/*
+ * Top k of one row of n scores (the "TopK" of the indexer method): the k
+ * largest, ties broken by the lower index, returned in ascending index order
+ * (k >= n: every index).  A NaN score ranks below every number, -inf included.
+ * A plain selection: repeatedly take the best remaining entry.  Returns the count.
+ */
+static int cmp_long(const void *a, const void *b) {
+    const long x = *(const long *)a, y = *(const long *)b;
+    return (x > y) - (x < y);
+}
+static int ranks_above(double a, double b) {
+    if (isnan(a)) return 0;
+    if (isnan(b)) return 1;
+    return a > b;
+}
+long oracle_topk_row(const double *s, long n, long k, long *out) {
+    const long take = k < n ? (k > 0 ? k : 0) : n;
+    char *used = (char *)calloc((size_t)(n > 0 ? n : 1), 1);
+    for (long j = 0; j < take; ++j) {
+        long best = -1;
+        for (long t = 0; t < n; ++t) {
+            if (used[t]) continue;
+            if (best < 0 || ranks_above(s[t], s[best])) best = t;  /* strict: the lowest index wins ties */
+        }
+        used[best] = 1;
+        out[j] = best;
+    }
+    free(used);
+    qsort(out, (size_t)take, sizeof(long), cmp_long);
+    return take;
+}
