@@ -60,6 +60,8 @@ typedef enum {
                                          block table */
 #define MLA_DEV_WAIT_TIMEOUT    0x4u  /* an on-chip wait gave up (kernel bailed out) */
 #define MLA_DEV_PLAN_OVERFLOW   0x8u  /* the split plan did not fit the workspace */
+#define MLA_DEV_SELECT_OVERFLOW 0x10u /* the top-k selection counted more than k picks (an internal
+                                         inconsistency; the extra picks are dropped, never written) */
 
 /*
  * mla_absorb_q - move the content query into latent space (explainer Step 6,
@@ -233,6 +235,83 @@ mla_status_t mla_cache_append_compressed(const void *h, const void *w_dkv, const
                                          const int32_t *block_table, const int32_t *seq_lens, int batch,
                                          int n_blocks, int m, int d_model, int num_pages, int max_pages,
                                          float rope_base, void *kv_pool, mla_stream_t stream);
+
+/*
+ * The indexer path (the DeepSeek page, "KV cache data movement minimization"):
+ * every cached token also keeps a small index vector k_idx, paged exactly like
+ * the latent cache (same block table, same 64-token pages).  A decoding token
+ * scores every cached token with one dot product against its index query q_idx,
+ * keeps the k best, and attends over those tokens only, so the latent rows read
+ * are k per sequence instead of L_b.  The pages leave the query side of the
+ * index score open; the reading taken is a per-sequence index query of the
+ * index vectors' width, supplied by the caller.
+ *
+ * mla_index_scores - the index scores of every cached token:
+ *     scores[b, t] = q_idx[b, :] . idx_pool[block_table[b, t / 64], t % 64, :]
+ * for t < L_b = seq_lens[b] (fp32 products and sums); entries t >= L_b are not
+ * written.  A token on a page outside [0, num_pages) gets a NaN score and sets
+ * MLA_DEV_BAD_BLOCK_TABLE.
+ *
+ * q_idx        [batch, d_idx] bf16
+ * idx_pool     [num_pages, 64, d_idx] bf16
+ * block_table  [batch, max_pages] int32, device; seq_lens [batch] int32, device
+ * scores       [batch, max_pages * 64] float32 (output)
+ * Limits: d_idx in {32, 64, 128, 256}; 1 <= batch <= 65536.
+ */
+mla_status_t mla_index_scores(const void *q_idx, const void *idx_pool, const int32_t *block_table,
+                              const int32_t *seq_lens, int batch, int d_idx, int num_pages, int max_pages,
+                              float *scores, mla_stream_t stream);
+
+/*
+ * mla_topk_gather - the k best tokens of each sequence and their cache rows.
+ * Sequence b selects the min(k, L_b) positions with the largest scores[b, t],
+ * t < L_b; equal scores go to the lower position first, and a NaN score ranks
+ * below every number (-inf included).  Outputs:
+ *     sel_index[b, 0:n]        the selected positions, ascending; -1 after them
+ *     sel_pool[b*npk + j]      page j of sequence b's selected rows, npk = ceil(k / 64):
+ *                              row i is kv_pool's row of position sel_index[b, i];
+ *                              rows i >= n are zero
+ *     sel_block_table[b, j]    b * npk + j
+ *     sel_lens[b]              n = min(k, L_b)
+ * so mla_decode(q_abs, sel_pool, sel_block_table, sel_lens, ..., num_pages = batch * npk,
+ * max_pages = npk, causal = 0) attends over exactly the selected tokens.
+ *
+ * scores           [batch, max_pages * 64] float32 (from mla_index_scores)
+ * kv_pool          [num_pages, 64, 576] bf16; block_table [batch, max_pages] int32
+ * sel_index        [batch, k] int32; sel_pool [batch * npk, 64, 576] bf16;
+ * sel_block_table  [batch, npk] int32; sel_lens [batch] int32 (all outputs, device)
+ * A selected row on a page outside [0, num_pages) is written as zeros and sets
+ * MLA_DEV_BAD_BLOCK_TABLE.
+ * Limits: 1 <= k <= 2^18; 1 <= batch <= 65536.
+ */
+mla_status_t mla_topk_gather(const float *scores, const int32_t *seq_lens, const void *kv_pool,
+                             const int32_t *block_table, int batch, int num_pages, int max_pages, int k,
+                             int32_t *sel_index, void *sel_pool, int32_t *sel_block_table, int32_t *sel_lens,
+                             mla_stream_t stream);
+
+/*
+ * mla_decode_sparse_workspace_size - bytes of workspace mla_decode_sparse needs
+ * (the scores, the selection and its compact pool, and mla_decode's workspace).
+ * Returns 0 for invalid sizes.
+ */
+size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k);
+
+/*
+ * mla_decode_sparse - the indexer decode of one new token per sequence:
+ * mla_index_scores, mla_topk_gather, then mla_decode (non-causal) over the
+ * selected rows: for every sequence b and head h,
+ *     o_lat[b, 0, h] = sum_{t in S_b} softmax_t(scale * q_abs[b, 0, h] . row_t) row_t[0:512]
+ *     lse[b, 0, h]   = log sum_{t in S_b} exp(scale * q_abs[b, 0, h] . row_t)
+ * where S_b = the selected positions.  q_abs [batch, 1, 128, 576] bf16; sel_index
+ * [batch, k] int32 receives the selection when not NULL.  Other arguments as above
+ * and as mla_decode; workspace of at least mla_decode_sparse_workspace_size() bytes,
+ * 16-byte aligned, not shared by overlapping calls.  Five kernels are enqueued.
+ */
+mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
+                               const int32_t *block_table, const int32_t *seq_lens, int batch, int n_heads,
+                               int d_idx, int num_pages, int max_pages, int k, float scale, void *o_lat,
+                               float *lse, int32_t *sel_index, void *workspace, size_t workspace_bytes,
+                               mla_stream_t stream);
 
 /*
  * mla_get_device_status - synchronise `stream`, then read and clear the

@@ -35,6 +35,7 @@ DEV_BAD_BLOCK_TABLE = 0x1
 DEV_BAD_SEQ_LEN = 0x2
 DEV_WAIT_TIMEOUT = 0x4
 DEV_PLAN_OVERFLOW = 0x8
+DEV_SELECT_OVERFLOW = 0x10
 
 
 class Status(enum.IntEnum):
@@ -67,6 +68,11 @@ EXPORTS = {
     "mla_up_proj": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "mla_cache_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _VP]),
     "mla_cache_append_compressed": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP]),
+    "mla_index_scores": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
+    "mla_topk_gather": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "mla_decode_sparse_workspace_size": (_SZ, [_I, _I, _I]),
+    "mla_decode_sparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _VP, _SZ,
+                               _VP]),
     "mla_get_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "mla_cache_bytes": (ctypes.c_uint64, [ctypes.c_int64, _I, _I, _I, _I]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
@@ -271,6 +277,89 @@ def combine(o_parts, lse_parts, o_out=None, lse_out=None, stream=None):
     _check(lib().mla_combine(_ptr(o_parts), _ptr(lse_parts), R, rows, _ptr(o_out), _ptr(lse_out),
                              _stream(stream)), "mla_combine")
     return o_out, lse_out
+
+
+def index_scores(q_idx, idx_pool, block_table, seq_lens, scores=None, stream=None):
+    """Index scores of every cached token: scores[b, t] = q_idx[b] . idx_pool[block_table[b, t // 64], t % 64]
+    for t < seq_lens[b] (later entries are not written).  q_idx [B, d_idx] bf16, idx_pool [P, 64, d_idx]
+    bf16.  Returns scores [B, max_pages * 64] f32."""
+    import torch
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(idx_pool, torch.bfloat16, "idx_pool")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, d_idx = q_idx.shape
+    max_pages = block_table.shape[1]
+    if scores is None:
+        scores = torch.empty(B, max_pages * PAGE, dtype=torch.float32, device=q_idx.device)
+    _need(scores, torch.float32, "scores")
+    _check(lib().mla_index_scores(_ptr(q_idx), _ptr(idx_pool), _ptr(block_table), _ptr(seq_lens), B, d_idx,
+                                  idx_pool.shape[0], max_pages, _ptr(scores), _stream(stream)), "mla_index_scores")
+    return scores
+
+
+def topk_gather(scores, seq_lens, kv_pool, block_table, k: int, stream=None):
+    """The k best-scored tokens of each sequence (ties: lower position; NaN last) and their cache rows.
+
+    Returns (sel_index [B, k] int32, sel_pool [B * npk, 64, 576] bf16, sel_block_table [B, npk] int32,
+    sel_lens [B] int32), npk = ceil(k / 64)."""
+    import torch
+    _need(scores, torch.float32, "scores")
+    _need(kv_pool, torch.bfloat16, "kv_pool")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, max_pages = block_table.shape
+    npk = (int(k) + PAGE - 1) // PAGE
+    dev = scores.device
+    sel_index = torch.empty(B, max(1, int(k)), dtype=torch.int32, device=dev)
+    sel_pool = torch.empty(max(1, B * npk), PAGE, D, dtype=torch.bfloat16, device=dev)
+    sel_bt = torch.empty(B, max(1, npk), dtype=torch.int32, device=dev)
+    sel_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib().mla_topk_gather(_ptr(scores), _ptr(seq_lens), _ptr(kv_pool), _ptr(block_table), B,
+                                 kv_pool.shape[0], max_pages, int(k), _ptr(sel_index), _ptr(sel_pool), _ptr(sel_bt),
+                                 _ptr(sel_lens), _stream(stream)), "mla_topk_gather")
+    return sel_index, sel_pool, sel_bt, sel_lens
+
+
+def decode_sparse_workspace_size(batch: int, max_pages: int, k: int) -> int:
+    return int(lib().mla_decode_sparse_workspace_size(batch, max_pages, k))
+
+
+def decode_sparse(q_abs, q_idx, kv_pool, idx_pool, block_table, seq_lens, k: int, scale: float = SCALE,
+                  o_lat=None, lse=None, sel_index=None, workspace=None, stream=None) -> Tuple:
+    """The indexer decode of one new token per sequence: index scores, top k, the decode over the k
+    selected tokens.  q_abs [B, 1, 128, 576] bf16, q_idx [B, d_idx] bf16, idx_pool [P, 64, d_idx] bf16.
+    Returns (o_lat [B, 1, 128, 512] bf16, lse [B, 1, 128] f32, sel_index [B, k] int32)."""
+    import torch
+    _need(q_abs, torch.bfloat16, "q_abs")
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(kv_pool, torch.bfloat16, "kv_pool")
+    _need(idx_pool, torch.bfloat16, "idx_pool")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Tq, nh, _ = q_abs.shape
+    if Tq != 1:
+        raise ValueError("decode_sparse: one new token per sequence (q_abs [B, 1, 128, 576])")
+    dev = q_abs.device
+    if o_lat is None:
+        o_lat = torch.empty(B, 1, nh, D_C, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(B, 1, nh, dtype=torch.float32, device=dev)
+    if sel_index is None:
+        sel_index = torch.empty(B, max(1, int(k)), dtype=torch.int32, device=dev)
+    _need(o_lat, torch.bfloat16, "o_lat")
+    _need(lse, torch.float32, "lse")
+    _need(sel_index, torch.int32, "sel_index")
+    max_pages = block_table.shape[1]
+    if workspace is None:
+        workspace = torch.empty(max(1, decode_sparse_workspace_size(B, max_pages, int(k))), dtype=torch.uint8,
+                                device=dev)
+    st = lib().mla_decode_sparse(_ptr(q_abs), _ptr(q_idx), _ptr(kv_pool), _ptr(idx_pool), _ptr(block_table),
+                                 _ptr(seq_lens), B, nh, q_idx.shape[1], kv_pool.shape[0], max_pages, int(k),
+                                 float(scale), _ptr(o_lat), _ptr(lse), _ptr(sel_index), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "mla_decode_sparse")
+    return o_lat, lse, sel_index
 
 
 def get_device_status(stream=None) -> Tuple[int, int]:

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmla.so")
 SOURCES = [os.path.join(CSRC, "mla.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "decode_kernels.cuh", "gemm_kernels.cuh", "append_kernels.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "decode_kernels.cuh", "gemm_kernels.cuh", "append_kernels.cuh",
+                                                   "sparse_kernels.cuh")] + [
     os.path.join(ROOT, "include", "mla.h"), os.path.join(ROOT, "include", "mla_testing.h")]
 
 

@@ -1,7 +1,7 @@
 // mla.cu - C ABI of the MLA decode library (declared in include/mla.h).
 // Host side only: argument checks, TMA descriptors, launch configuration.
-// Every numeric step runs in the kernels of decode_kernels.cuh, gemm_kernels.cuh and
-// append_kernels.cuh.
+// Every numeric step runs in the kernels of decode_kernels.cuh, gemm_kernels.cuh,
+// append_kernels.cuh and sparse_kernels.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -16,6 +16,7 @@
 #include "append_kernels.cuh"
 #include "decode_kernels.cuh"
 #include "gemm_kernels.cuh"
+#include "sparse_kernels.cuh"
 
 namespace mla {
 namespace {
@@ -79,7 +80,9 @@ mla_status_t device_setup(int *dev_out, DeviceInfo **info_out) {
                 cudaFuncSetAttribute(append_kernel<64, 64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)AppendShape<64, 64>::kSmem) != cudaSuccess ||
                 cudaFuncSetAttribute(append_kernel<64, 128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)AppendShape<64, 128>::kSmem) != cudaSuccess)
+                                     (int)AppendShape<64, 128>::kSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(topk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kTopkStageKeys * sizeof(uint32_t))) != cudaSuccess)
                 return MLA_ERR_CUDA;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
@@ -278,6 +281,37 @@ mla_status_t launch_error(uint64_t kernels = 1) {
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     g_launches += kernels;
     return MLA_OK;
+}
+
+constexpr int kMaxTopK = 1 << 18;
+
+// Workspace of the indexer decode: scores, selection, compact pool and its table, then the
+// decode's own workspace.
+struct SparseWs {
+    size_t scores, sel_index, sel_pool, sel_bt, sel_lens, dec, dec_bytes, total;
+    int npk;
+};
+bool sparse_ws_layout(int batch, int max_pages, int k, SparseWs *w) {
+    if (batch < 1 || batch > kMaxRows || max_pages < 1 || k < 1 || k > kMaxTopK) return false;
+    if ((long long)max_pages * kPage > 0x7fffffffll) return false;
+    w->npk = (k + kPage - 1) / kPage;
+    const size_t dec = mla_decode_workspace_size(batch, 1, 0);
+    if (dec == 0) return false;
+    size_t off = 0;
+    w->scores = off;
+    off = align_up(off + sizeof(float) * (size_t)batch * max_pages * kPage, 256);
+    w->sel_index = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)batch * k, 256);
+    w->sel_pool = off;
+    off = align_up(off + (size_t)batch * w->npk * kPage * kSparseRow * 2, 256);
+    w->sel_bt = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)batch * w->npk, 256);
+    w->sel_lens = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)batch, 256);
+    w->dec = off;
+    w->dec_bytes = dec;
+    w->total = off + dec;
+    return true;
 }
 
 // Device address of the library-owned decode scratch on each device, looked up once.
@@ -692,6 +726,141 @@ mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_par
     combine_rows_kernel<<<(rows + kCombineHeads - 1) / kCombineHeads, kCombineThreads, 0, (cudaStream_t)stream>>>(
         o_parts, lse_parts, n_parts, rows, static_cast<__nv_bfloat16 *>(o_out), lse_out);
     return launch_error();
+}
+
+mla_status_t mla_index_scores(const void *q_idx, const void *idx_pool, const int32_t *block_table,
+                              const int32_t *seq_lens, int batch, int d_idx, int num_pages, int max_pages,
+                              float *scores, mla_stream_t stream) {
+    if (!q_idx || !idx_pool || !block_table || !seq_lens || !scores) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || num_pages < 1 || max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (d_idx != 32 && d_idx != 64 && d_idx != 128 && d_idx != 256) return MLA_ERR_SHAPE;
+    if (batch > kMaxRows || (long long)max_pages * kPage > 0x7fffffffll ||
+        (long long)num_pages * kPage * d_idx > (1ll << 40))
+        return MLA_ERR_SHAPE;
+    if (!aligned16(q_idx) || !aligned16(idx_pool) || !aligned4(scores) || !aligned4(block_table) ||
+        !aligned4(seq_lens))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    // about 32 warps per SM over the whole batch, each taking a few pages of one sequence
+    const long long warps = (long long)info->sms * 32;
+    const long long pages = (long long)batch * max_pages;
+    const long long per_warp = pages <= warps ? 1 : (pages + warps - 1) / warps;
+    const int wpc = kScoreThreads / 32;
+    const int cps = (int)((max_pages + wpc * per_warp - 1) / (wpc * per_warp));
+    ScoreParams p;
+    p.q_idx = static_cast<const __nv_bfloat16 *>(q_idx);
+    p.idx_pool = static_cast<const __nv_bfloat16 *>(idx_pool);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.scores = scores;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.ctas_per_seq = cps;
+    const dim3 grid((unsigned)((long long)batch * cps));
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (d_idx) {
+        case 32: index_score_kernel<4><<<grid, kScoreThreads, 0, s>>>(p); break;
+        case 64: index_score_kernel<8><<<grid, kScoreThreads, 0, s>>>(p); break;
+        case 128: index_score_kernel<16><<<grid, kScoreThreads, 0, s>>>(p); break;
+        default: index_score_kernel<32><<<grid, kScoreThreads, 0, s>>>(p); break;
+    }
+    return launch_error();
+}
+
+mla_status_t mla_topk_gather(const float *scores, const int32_t *seq_lens, const void *kv_pool,
+                             const int32_t *block_table, int batch, int num_pages, int max_pages, int k,
+                             int32_t *sel_index, void *sel_pool, int32_t *sel_block_table, int32_t *sel_lens,
+                             mla_stream_t stream) {
+    if (!scores || !seq_lens || !kv_pool || !block_table || !sel_index || !sel_pool || !sel_block_table || !sel_lens)
+        return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || num_pages < 1 || max_pages < 1 || k < 1) return MLA_ERR_INVALID_ARG;
+    if (k > kMaxTopK || batch > kMaxRows || (long long)max_pages * kPage > 0x7fffffffll) return MLA_ERR_SHAPE;
+    if (!aligned16(scores) || !aligned16(kv_pool) || !aligned16(sel_pool) || !aligned4(seq_lens) ||
+        !aligned4(block_table) || !aligned4(sel_index) || !aligned4(sel_block_table) || !aligned4(sel_lens))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    TopkParams p;
+    p.scores = scores;
+    p.seq_lens = seq_lens;
+    p.kv_pool = static_cast<const __nv_bfloat16 *>(kv_pool);
+    p.block_table = block_table;
+    p.sel_index = sel_index;
+    p.sel_pool = static_cast<__nv_bfloat16 *>(sel_pool);
+    p.sel_block_table = sel_block_table;
+    p.sel_lens = sel_lens;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.k = k;
+    p.npk = (k + kPage - 1) / kPage;
+    // the largest slice any CTA can own (a sequence of max_pages * 64 tokens): staged in shared
+    // memory when it fits
+    const long long max_chunk = (((long long)max_pages * kPage + kTopkCluster - 1) / kTopkCluster + 3) & ~3ll;
+    p.staged = max_chunk <= kTopkStageKeys ? 1 : 0;
+    const size_t dyn = p.staged ? (size_t)max_chunk * sizeof(uint32_t) : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(batch * kTopkCluster), 1, 1);
+    cfg.blockDim = dim3(kTopkThreads, 1, 1);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kTopkCluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_gather_kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    g_launches += 1;
+    return MLA_OK;
+}
+
+size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k) {
+    SparseWs w;
+    if (!sparse_ws_layout(batch, max_pages, k, &w)) return 0;
+    return w.total;
+}
+
+mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
+                               const int32_t *block_table, const int32_t *seq_lens, int batch, int n_heads,
+                               int d_idx, int num_pages, int max_pages, int k, float scale, void *o_lat,
+                               float *lse, int32_t *sel_index, void *workspace, size_t workspace_bytes,
+                               mla_stream_t stream) {
+    if (!q_abs || !q_idx || !kv_pool || !idx_pool || !block_table || !seq_lens || !o_lat || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || num_pages < 1 || max_pages < 1 || k < 1) return MLA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+    if (n_heads != kHeads) return MLA_ERR_UNSUPPORTED;
+    if (d_idx != 32 && d_idx != 64 && d_idx != 128 && d_idx != 256) return MLA_ERR_SHAPE;
+    SparseWs w;
+    if (!sparse_ws_layout(batch, max_pages, k, &w)) return MLA_ERR_SHAPE;
+    if ((long long)batch * w.npk > 0x7fffffffll / kPage) return MLA_ERR_SHAPE;
+    if (!workspace || workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace) || !aligned16(q_abs) || !aligned16(o_lat) || !aligned4(lse) ||
+        (sel_index && !aligned4(sel_index)))
+        return MLA_ERR_ALIGNMENT;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *scores = reinterpret_cast<float *>(ws + w.scores);
+    int32_t *sel = sel_index ? sel_index : reinterpret_cast<int32_t *>(ws + w.sel_index);
+    void *sel_pool = ws + w.sel_pool;
+    int32_t *sel_bt = reinterpret_cast<int32_t *>(ws + w.sel_bt);
+    int32_t *sel_lens = reinterpret_cast<int32_t *>(ws + w.sel_lens);
+    mla_status_t st = mla_index_scores(q_idx, idx_pool, block_table, seq_lens, batch, d_idx, num_pages, max_pages,
+                                       scores, stream);
+    if (st != MLA_OK) return st;
+    st = mla_topk_gather(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool,
+                         sel_bt, sel_lens, stream);
+    if (st != MLA_OK) return st;
+    return mla_decode(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, n_heads, batch * w.npk, w.npk, scale, 0, 0,
+                      o_lat, lse, ws + w.dec, w.dec_bytes, stream);
 }
 
 mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream) {

@@ -3,6 +3,7 @@ without it).
 
   python -m mla_latent_kv_77_b300.trace [--workload NAME] [--out FILE.npz]
   python -m mla_latent_kv_77_b300.trace --append NAME [--out FILE.npz]
+  python -m mla_latent_kv_77_b300.trace --topk NAME [--out FILE.npz]
 
 builds ``libmla_trace.so`` from the same sources with ``-DMLA_TRACE`` (every role of the decode
 and cache-write kernels then stamps its waits and issues with the SM cycle counter, see ``Tracer``
@@ -166,6 +167,71 @@ def summarize_append(path: str, mhz: float = 2032.0) -> str:
     return "\n".join(lines)
 
 
+def record_topk(workload: str, out: str) -> str:
+    import torch
+    import mla_latent_kv_77_b300 as mla
+    from mla_latent_kv_77_b300 import workloads
+    if mla._lib is not None:
+        raise RuntimeError("the untraced library is already loaded in this process")
+    mla.LIB_PATH = TRACE_LIB
+    lib = mla.lib()
+    lib.mla_trace_set.restype = ctypes.c_int
+    lib.mla_trace_set.argtypes = [ctypes.c_void_p]
+    dev = torch.device("cuda")
+    sc = workloads.make_sparse_workload(workload, seed=0, device=dev)
+    c = sc.case
+    bt, sl = c.block_table.to(dev), c.seq_lens.to(dev)
+    scores = mla.index_scores(sc.q_idx, sc.idx_pool, bt, sl)
+    n_cta = max(148, c.B * TOPK_CLUSTER)
+    buf = torch.zeros(n_cta * WARPS * SLOTS, dtype=torch.int64, device=dev)
+    for _ in range(3):
+        mla.topk_gather(scores, sl, c.pool, bt, sc.k)
+    torch.cuda.synchronize()
+    if lib.mla_trace_set(ctypes.c_void_p(buf.data_ptr())) != 0:
+        raise RuntimeError("mla_trace_set failed")
+    mla.topk_gather(scores, sl, c.pool, bt, sc.k)
+    torch.cuda.synchronize()
+    lib.mla_trace_set(ctypes.c_void_p(0))
+    st, word = mla.get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {word:#x}")
+    np.savez_compressed(out, trace=buf.cpu().numpy(), workload=workload, kind="topk", n_cta=n_cta,
+                        busy=c.B * TOPK_CLUSTER)
+    return out
+
+
+TOPK_CLUSTER = 8
+# top-k steps (warp 0, global timer): (name, tag)
+TOPK_STEPS = [("keys staged", 0x8201)] + [(f"pass {i}: histogram counted", 0x8210 + i) for i in range(4)] + [
+    (f"pass {i}: cluster sum, bin chosen", 0x8220 + i) for i in range(4)] + [
+    ("output offsets known", 0x8231), ("positions written", 0x8232), ("rows' pool offsets", 0x8233),
+    ("rows copied", 0x8234)]
+
+
+def summarize_topk(path: str) -> str:
+    d = np.load(path)
+    n_cta, busy = int(d["n_cta"]), int(d["busy"])
+    tr = d["trace"].reshape(n_cta, WARPS, SLOTS)
+    starts = []
+    for b in range(busy):
+        tags, t = _events(tr, b, 0)
+        if (tags == 0x8200).any():
+            starts.append(t[tags == 0x8200][0])
+    t_first = min(starts)
+    lines = [f"{path}: {busy} CTAs; us after the first CTA's start (global timer): median (max) over CTAs"]
+    lines.append(f"  {'start':34s} {np.median((np.array(starts) - t_first) / 1e3):7.3f} "
+                 f"({(max(starts) - t_first) / 1e3:.3f})")
+    for name, tag in TOPK_STEPS:
+        xs = []
+        for b in range(busy):
+            tags, t = _events(tr, b, 0)
+            if (tags == tag).any():
+                xs.append((t[tags == tag][0] - t_first) / 1e3)
+        if xs:
+            lines.append(f"  {name:34s} {np.median(xs):7.3f} ({np.max(xs):.3f})")
+    return "\n".join(lines)
+
+
 def _events(tr, cta, warp):
     x = tr[cta, warp]
     x = x[x != 0]
@@ -213,13 +279,19 @@ def main():
     ap.add_argument("--workload", default="b64_l4096")
     ap.add_argument("--out", default=None)
     ap.add_argument("--append", default=None, help="trace the cache write on this workload instead")
+    ap.add_argument("--topk", default=None, help="trace the top-k selection on this indexer workload instead")
     ap.add_argument("--summarize", default=None, help="only summarise an existing record")
     args = ap.parse_args()
     if args.summarize:
         kind = str(np.load(args.summarize).get("kind", "decode"))
-        print(summarize_append(args.summarize) if kind == "append" else summarize(args.summarize))
+        print({"append": summarize_append, "topk": summarize_topk}.get(kind, summarize)(args.summarize))
         return 0
     build()
+    if args.topk:
+        out = args.out or f"trace_{args.topk}.npz"
+        record_topk(args.topk, out)
+        print(summarize_topk(out))
+        return 0
     if args.append:
         out = args.out or f"trace_{args.append}.npz"
         record_append(args.append, out)

@@ -23,6 +23,10 @@ reproducible on its own; the ragged lengths come first, from a generator seeded
   k=10 W^DKV        ~ N(0, 1) / sqrt(d_model), bf16   (so c ~ N(0, 1))
   k=11 W^KR         ~ N(0, 1) / sqrt(d_model), bf16
   k=12 W^Z (compressed cache write) ~ N(0, 1) / sqrt(d_model), bf16
+  k=13 index cache (indexer decode) ~ N(0, 1) / sqrt(d_idx), bf16, one d_idx-wide vector per
+       pool row; with ``ties`` set, instead integers uniform in [-2, 2] (many exactly equal
+       scores, to exercise the tie rule)
+  k=14 q_idx        ~ N(0, 1), bf16 (with ``ties``: integers uniform in [-2, 2])
 
 Shapes follow the DeepSeek-V2 attention: 128 heads, 512-d latent, 64-d decoupled
 RoPE key, 128-d head, 576-number cache row, 64-token pages.
@@ -294,3 +298,55 @@ COMPRESS_WORKLOADS = {
 
 def make_compress_workload(name: str, seed: int = 0, device="cpu") -> CompressCase:
     return make_compress_case(name, seed=seed, device=device, **COMPRESS_WORKLOADS[name])
+
+
+D_IDX = 128  # index vector width of the indexer workloads (the pages give none)
+
+
+@dataclass
+class SparseCase:
+    """An indexer decode: a decode case plus the paged index cache and the index queries."""
+    case: Case                      # pool, block table, lengths, q_abs
+    idx_pool: torch.Tensor          # [num_pages, PAGE, d_idx] bf16
+    q_idx: torch.Tensor             # [B, d_idx] bf16
+    k: int
+
+    @property
+    def d_idx(self) -> int:
+        return int(self.idx_pool.shape[2])
+
+    def index_bytes(self) -> int:
+        """Bytes of index cache one step reads (each visible token's vector once)."""
+        return int(self.case.seq_lens.to(torch.int64).sum()) * self.d_idx * 2
+
+    def selected_bytes(self) -> int:
+        """Bytes of latent cache rows the selection gathers: min(k, L_b) rows per sequence."""
+        return int(self.case.seq_lens.clamp(max=self.k).to(torch.int64).sum()) * D * 2
+
+
+def make_sparse_case(name: str, seq_lens: List[int], k: int, d_idx: int = D_IDX, ties: bool = False,
+                     shuffle: bool = False, spare_pages: int = 0, garbage: Optional[str] = None,
+                     peaked_frac: float = 0.0, seed: int = 0, device="cpu") -> SparseCase:
+    case = make_case(name, seq_lens, Tq=1, causal=False, shuffle=shuffle, spare_pages=spare_pages,
+                     garbage=garbage, peaked_frac=peaked_frac, q_mode="abs", seed=seed, device=device)
+    shape = (case.num_pages, PAGE, d_idx)
+    if ties:
+        idx = torch.randint(-2, 3, shape, generator=_gen(seed, 13, device), device=device).to(torch.bfloat16)
+        q_idx = torch.randint(-2, 3, (case.B, d_idx), generator=_gen(seed, 14, device), device=device)
+        q_idx = q_idx.to(torch.bfloat16)
+    else:
+        idx = _randn_bf16(shape, 1.0 / math.sqrt(d_idx), seed, 13, device)
+        q_idx = _randn_bf16((case.B, d_idx), 1.0, seed, 14, device)
+    return SparseCase(case=case, idx_pool=idx, q_idx=q_idx, k=int(k))
+
+
+# Indexer decode workloads: the 128K-token batch with the page's top-k of 512.
+SPARSE_WORKLOADS = {
+    # batch 8 x 131072 tokens (1% of rows peaked, as the dense 128K workload), top 512 by a
+    # 128-wide index vector per token
+    "sparse_b8_l128k_k512": dict(seq_lens=[131072] * 8, k=512, peaked_frac=0.01),
+}
+
+
+def make_sparse_workload(name: str, seed: int = 0, device="cpu") -> SparseCase:
+    return make_sparse_case(name, seed=seed, device=device, **SPARSE_WORKLOADS[name])

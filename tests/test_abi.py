@@ -171,6 +171,53 @@ def test_cache_append_compressed_rejects_bad_arguments_on_host(lib):
     assert call(pool=104) == mla.Status.ALIGNMENT
 
 
+def test_indexer_calls_reject_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+
+    def scores(d_idx=128, B=2, q=16, pool=32, sc=64):
+        return lib.mla_index_scores(vp(q) if q else None, vp(pool), vp(48), vp(80), B, d_idx, 4, 2,
+                                    vp(sc) if sc else None, None)
+    assert scores(q=None) == mla.Status.INVALID_ARG
+    assert scores(sc=None) == mla.Status.INVALID_ARG
+    assert scores(B=0) == mla.Status.INVALID_ARG
+    for d in (0, 16, 96, 512):
+        assert scores(d_idx=d) == mla.Status.SHAPE
+    assert scores(q=24) == mla.Status.ALIGNMENT
+    assert scores(pool=40) == mla.Status.ALIGNMENT
+    assert scores(sc=66) == mla.Status.ALIGNMENT
+
+    def topk(k=512, B=2, sc=16, pool=32, sp=48, si=64):
+        return lib.mla_topk_gather(vp(sc), vp(80), vp(pool), vp(96), B, 4, 2, k, vp(si) if si else None, vp(sp),
+                                   vp(112), vp(128), None)
+    assert topk(si=None) == mla.Status.INVALID_ARG
+    assert topk(k=0) == mla.Status.INVALID_ARG
+    assert topk(B=0) == mla.Status.INVALID_ARG
+    assert topk(k=(1 << 18) + 1) == mla.Status.SHAPE
+    assert topk(sc=20) == mla.Status.ALIGNMENT
+    assert topk(sp=56) == mla.Status.ALIGNMENT
+    assert topk(pool=40) == mla.Status.ALIGNMENT
+
+    assert lib.mla_decode_sparse_workspace_size(0, 4, 512) == 0
+    assert lib.mla_decode_sparse_workspace_size(2, 4, 0) == 0
+    assert lib.mla_decode_sparse_workspace_size(2, 4, (1 << 18) + 1) == 0
+    need = lib.mla_decode_sparse_workspace_size(8, 2048, 512)
+    # at least the scores, the selection, the compact pool and the decode's own workspace
+    assert need >= 8 * 2048 * 64 * 4 + 8 * 512 * 4 + 8 * 8 * 64 * 576 * 2 + lib.mla_decode_workspace_size(8, 1, 0)
+
+    def sparse(k=512, nh=128, d_idx=128, ws=256, nbytes=None, scale=0.07, qa=16):
+        nb = need if nbytes is None else nbytes
+        return lib.mla_decode_sparse(vp(qa), vp(32), vp(48), vp(64), vp(80), vp(96), 8, nh, d_idx, 4096, 2048, k,
+                                     scale, vp(112), vp(128), None, vp(ws) if ws else None, nb, None)
+    assert sparse(ws=None) == mla.Status.WORKSPACE
+    assert sparse(nbytes=need - 1) == mla.Status.WORKSPACE
+    assert sparse(nh=64) == mla.Status.UNSUPPORTED
+    assert sparse(d_idx=100) == mla.Status.SHAPE
+    assert sparse(k=0) == mla.Status.INVALID_ARG
+    assert sparse(scale=0.0) == mla.Status.INVALID_ARG
+    assert sparse(ws=264) == mla.Status.ALIGNMENT
+    assert sparse(qa=20) == mla.Status.ALIGNMENT
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mla, "_lib", None)
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
