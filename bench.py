@@ -502,6 +502,71 @@ def other_workloads_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_in
     return res
 
 
+def sparse_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_index: int = 0) -> dict:
+    """The indexer decode (mla_decode_sparse: index scores over every cached token, top k, the
+    decode over the k selected rows) on the batch-8, 131072-token workload with k = 512 and a
+    128-wide index vector per token.  The whole call is timed as the headline decode is (K calls
+    back to back between one event pair, two alternating caches of index vectors and latent rows,
+    both larger than L2); each of its two own kernels alone is captured into a CUDA graph and
+    replayed (the index scores alternating between the two index caches).  Roofline of the call:
+    the index vectors it must read plus the selected rows; of the score kernel: the index vectors."""
+    import torch
+    name = "sparse_b8_l128k_k512"
+    sc = workloads.make_sparse_workload(name, seed=0, device=dev)
+    c = sc.case
+    stream = torch.cuda.current_stream()
+    pools = [c.pool, c.pool.clone()]
+    idxs = [sc.idx_pool, sc.idx_pool.clone()]
+    bt, sl = c.block_table.to(dev), c.seq_lens.to(dev)
+    o = torch.empty(c.B, 1, 128, 512, dtype=torch.bfloat16, device=dev)
+    l = torch.empty(c.B, 1, 128, dtype=torch.float32, device=dev)
+    si = torch.empty(c.B, sc.k, dtype=torch.int32, device=dev)
+    ws = torch.empty(mla.decode_sparse_workspace_size(c.B, c.max_pages, sc.k), dtype=torch.uint8, device=dev)
+
+    def call(i, st=None):
+        mla.decode_sparse(c.q_abs, sc.q_idx, pools[i & 1], idxs[i & 1], bt, sl, sc.k, c.scale, o_lat=o, lse=l,
+                          sel_index=si, workspace=ws, stream=st or stream)
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize()
+    n0 = mla.launch_count()
+    with ClockSampler(gpu_index) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clk.mark_begin()
+        e0.record(stream)
+        for i in range(steps):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clk.mark_end()
+    launches = (mla.launch_count() - n0) // steps
+    us = e0.elapsed_time(e1) * 1000.0 / steps
+    scores = torch.empty(c.B, c.max_pages * 64, dtype=torch.float32, device=dev)
+    score_us = graph_us([lambda st, k=k: mla.index_scores(sc.q_idx, idxs[k], bt, sl, scores=scores, stream=st)
+                         for k in range(2)], max(1, steps // 2))
+    mla.index_scores(sc.q_idx, idxs[0], bt, sl, scores=scores)
+    sel = mla.topk_gather(scores, sl, pools[0], bt, sc.k)
+    topk_us = graph_us([lambda st: mla.lib().mla_topk_gather(
+        mla._ptr(scores), mla._ptr(sl), mla._ptr(pools[0]), mla._ptr(bt), c.B, c.num_pages, c.max_pages, sc.k,
+        mla._ptr(sel[0]), mla._ptr(sel[1]), mla._ptr(sel[2]), mla._ptr(sel[3]), mla._stream(st))], steps)
+    st_, word = mla.get_device_status()
+    assert st_ == 0, f"device status {word:#x}"
+    idx_bytes, sel_bytes = sc.index_bytes(), sc.selected_bytes()
+    call_bytes = idx_bytes + sel_bytes
+    res = {"workload": name, "batch": c.B, "context": int(c.seq_lens.max()), "k": sc.k, "d_idx": sc.d_idx,
+           "us": us, "tokens_per_s": c.B / (us * 1e-6), "launches_per_call": launches,
+           "call_bytes": call_bytes, "call_roofline_frac": call_bytes / (pk["hbm_gbs"] * 1e9) / (us * 1e-6),
+           "index_scores": {"us": score_us, "bytes": idx_bytes, "achieved_gbs": idx_bytes / (score_us * 1e-6) / 1e9,
+                            "frac": idx_bytes / (score_us * 1e-6) / 1e9 / pk["hbm_gbs"]},
+           "topk_gather_us": topk_us,
+           "timing": "whole call: K calls back to back between one event pair, two alternating caches; "
+                     "kernels alone: CUDA-graph replays",
+           "clocks": clk.summary()}
+    del sc, c, pools, idxs, ws, scores, sel
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each step
     decodes a bounded sample (`--ref-seqs` whole sequences, all heads and query tokens) of
@@ -556,6 +621,7 @@ def main():
     ap.add_argument("--no-fused", action="store_true", help="skip the fused absorb/decode/up-projection timing")
     ap.add_argument("--no-append", action="store_true", help="skip the cache-write timing")
     ap.add_argument("--no-others", action="store_true", help="skip the other large workloads' decode timing")
+    ap.add_argument("--no-sparse", action="store_true", help="skip the indexer (top-k sparse) decode timing")
     ap.add_argument("--ref-seqs", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -700,6 +766,10 @@ def main():
     if rank == 0 and world == 1 and args.workload == "b64_l4096" and not args.no_others:
         others = other_workloads_leg(mla, workloads, dev, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks(),
                                      gpu_index=local)
+    sparse = None
+    if rank == 0 and world == 1 and args.workload == "b64_l4096" and not args.no_sparse:
+        sparse = sparse_leg(mla, workloads, dev, steps=max(args.steps, 10), warmup=args.warmup, pk=peaks(),
+                            gpu_index=local)
     append = None
     if rank == 0 and args.workload == "b64_l4096" and not args.no_append:
         append = append_leg(mla, workloads, dev, stream, steps=max(args.steps, 20), warmup=args.warmup, pk=peaks())
@@ -740,6 +810,7 @@ def main():
             "fused": fused,
             "append": append,
             "other_workloads": others,
+            "sparse": sparse,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
