@@ -252,6 +252,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
     // it read carry them, so the output offsets need no exchange of their own.
     uint32_t prefix = 0, mask = 0, need = (uint32_t)p.k;  // need: keys still to take at the prefix
     if (!take_all) {
+        // rank q's keys in the chosen bins' upper neighbours so far (this thread's bin only); added
+        // over the block once, after the last pass
+        uint32_t acc_gt[kTopkCluster], acc_eq[kTopkCluster];
+#pragma unroll
+        for (int q = 0; q < kTopkCluster; ++q) acc_gt[q] = acc_eq[q] = 0u;
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
             if (pass > 0 || !staged) {
@@ -265,6 +270,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
             }
             tr.at(0x8210 + pass);
             cluster_sync_all();  // every CTA's histogram of this pass is complete
+            tr.at(0x8240 + pass);
             uint32_t h[kTopkCluster];
             if (tid < kTopkBins) {
                 const uint32_t a = smem_u32(&sm.hist[pass][tid]);
@@ -277,6 +283,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
             }
             if (pass == 3) cluster_arrive_relaxed();  // this CTA has read the others' shared memory
             __syncthreads();
+            tr.at(0x8250 + pass);
             // suffix sums from the top bin down: bin v holds the need-th largest key when the
             // keys in the bins above it number fewer than `need` and those with it at least `need`
             if (tid < kTopkBins) {
@@ -300,6 +307,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
                 }
             }
             __syncthreads();
+            tr.at(0x8260 + pass);
             const uint32_t v = sm.pick[0];
             need -= sm.pick[1];
             prefix |= v << shift;
@@ -308,21 +316,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
             if (tid < kTopkBins) {
 #pragma unroll
                 for (int q = 0; q < kTopkCluster; ++q) {
-                    uint32_t g = (uint32_t)tid > v ? h[q] : 0u;
-                    uint32_t e = (pass == 3 && (uint32_t)tid == v) ? h[q] : 0u;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        g += __shfl_xor_sync(0xffffffffu, g, off);
-                        e += __shfl_xor_sync(0xffffffffu, e, off);
-                    }
-                    if (lane == 0) {
-                        if (g) atomicAdd(&sm.rank_gt[q], g);
-                        if (e) atomicAdd(&sm.rank_eq[q], e);
-                    }
+                    acc_gt[q] += (uint32_t)tid > v ? h[q] : 0u;
+                    acc_eq[q] += (pass == 3 && (uint32_t)tid == v) ? h[q] : 0u;
                 }
             }
-            __syncthreads();  // pick[], warp_sum[] and the rank counts are complete
+            __syncthreads();  // pick[] and warp_sum[] are rewritten by the next pass
             tr.at(0x8220 + pass);
+        }
+        if (tid < kTopkBins) {
+#pragma unroll
+            for (int q = 0; q < kTopkCluster; ++q) {
+                if (acc_gt[q]) atomicAdd(&sm.rank_gt[q], acc_gt[q]);
+                if (acc_eq[q]) atomicAdd(&sm.rank_eq[q], acc_eq[q]);
+            }
         }
     } else if (tid < kTopkCluster) {
         // every position is taken: rank q's picks are its whole slice
