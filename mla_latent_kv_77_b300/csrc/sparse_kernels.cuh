@@ -29,10 +29,11 @@ constexpr int kSparseRow = 576;          // latent cache row: c (512) | k^R (64)
 constexpr int kScoreThreads = 256;
 constexpr int kScoreUnroll = 8;          // 16-byte loads in flight per lane
 constexpr int kTopkCluster = 8;          // CTAs per sequence (portable cluster size)
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkBins = 256;           // one byte of the key per pass
 constexpr int kTopkPickCap = 1024;   // picks per CTA whose positions are kept in shared memory
+constexpr int kTopkListCap = 128;    // positions per warp list (keys at or above the first pass's bin)
 
 // Order-keeping key of an fp32 score: larger score, larger key.  -0 is +0 (they tie), every NaN
 // maps to 0, below -inf's key (0x007FFFFF).
@@ -170,6 +171,10 @@ struct TopkSmem {
     uint32_t rank_eq[kTopkCluster]; //   from the histograms read during the passes
     uint32_t pick[2];               // the chosen bin, and the keys in bins above it
     int32_t slice_bt[kTopkSlicePages];  // block-table entries of the slice's pages
+    int32_t wlist[kTopkWarps][kTopkListCap];  // each warp's positions whose key's top byte is at
+                                              // least the first pass's chosen byte, in order
+    uint32_t wlist_n[kTopkWarps];
+    uint32_t list_overflow;
     int32_t pick_pos[kTopkPickCap]; // this CTA's first picks (positions), in output order
     int32_t src_row[kTopkPickCap];  // their pool rows (page * 64 + slot), -1 for a bad page
 };
@@ -208,11 +213,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
     const bool fits = p.staged != 0;                 // the slice fits the shared-memory copies
     const bool staged = fits && !take_all;
     const int page0 = lo / kSparsePage;
+    // warp w's sub-slice [wlo, whi): a multiple of 128 positions, 4 consecutive ones per lane per step
+    const int wspan = (((hi - lo) + kTopkWarps - 1) / kTopkWarps + 127) & ~127;
+    const int wlo = min(hi, lo + warp * wspan), whi = min(hi, wlo + wspan);
+    const uint32_t lt = (1u << lane) - 1u;
     Tracer tr;
     tr.at(0x8200);
 
     for (int i = tid; i < 4 * kTopkBins; i += kTopkThreads) (&sm.hist[0][0])[i] = 0u;
     if (tid < kTopkCluster) sm.rank_gt[tid] = sm.rank_eq[tid] = 0u;
+    if (tid == 0) sm.list_overflow = 0u;
     if (fits && hi > lo)
         for (int j = tid; j <= (hi - 1) / kSparsePage - page0; j += kTopkThreads)
             sm.slice_bt[j] = p.block_table[(size_t)b * p.max_pages + page0 + j];
@@ -259,7 +269,52 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
         for (int q = 0; q < kTopkCluster; ++q) acc_gt[q] = acc_eq[q] = 0u;
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            if (pass > 0 || !staged) {
+            if (pass == 1 && staged) {
+                // Scan the keys once more and keep, per warp and in position order, every position
+                // whose top byte is at least the first pass's chosen one: the keys that can still
+                // be picked (typically a few percent).  The later passes and the compaction read
+                // only these lists, unless one overflowed.
+                const uint32_t v0 = prefix >> 24;
+                uint32_t n = 0;
+                for (int e0 = wlo; e0 < whi; e0 += 128) {
+                    const int e = e0 + 4 * lane;
+                    uint32_t k4[4] = {0u, 0u, 0u, 0u};
+                    if (e < whi) topk_keys4(staged_keys, row, true, lo, e, k4);
+                    uint32_t in_bits = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t top = k4[i] >> 24;
+                        if (e + i < whi && top >= v0) {
+                            in_bits |= 1u << i;
+                            if (top == v0) atomicAdd(&sm.hist[1][(k4[i] >> 16) & 0xFFu], 1u);
+                        }
+                    }
+                    uint32_t slot = n, step = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t bal = __ballot_sync(0xffffffffu, (in_bits >> i) & 1u);
+                        slot += __popc(bal & lt);
+                        step += __popc(bal);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if ((in_bits >> i) & 1u) {
+                            if (slot < (uint32_t)kTopkListCap) sm.wlist[warp][slot] = e + i;
+                            ++slot;
+                        }
+                    n += step;
+                }
+                if (lane == 0) {
+                    sm.wlist_n[warp] = n;
+                    if (n > (uint32_t)kTopkListCap) sm.list_overflow = 1u;
+                }
+            } else if (pass >= 2 && staged && !sm.list_overflow) {
+                const uint32_t n = sm.wlist_n[warp];
+                for (uint32_t j = lane; j < n; j += 32) {
+                    const uint32_t key = staged_keys[sm.wlist[warp][j] - lo];
+                    if ((key & mask) == prefix) atomicAdd(&sm.hist[pass][(key >> shift) & 0xFFu], 1u);
+                }
+            } else if (pass > 0 || !staged) {
                 for (int e = lo + 4 * tid; e < hi; e += 4 * kTopkThreads) {
                     uint32_t k4[4];
                     topk_keys4(staged_keys, row, staged, lo, e, k4);
@@ -352,11 +407,63 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
     // `prefix` and equal to it, then writes its picks in position order after those of the lower
     // ranks and lower warps.
     int32_t *sel_out = p.sel_index + (size_t)b * p.k;
+    const bool use_lists = staged && !take_all && !sm.list_overflow;
     if (take_all) {
         for (int e = lo + tid; e < hi; e += kTopkThreads) sel_out[e] = e;
+    } else if (use_lists) {
+        // the same compaction over the warps' lists (every key above or equal to the threshold is
+        // in them, in position order)
+        const uint32_t n = sm.wlist_n[warp];
+        {
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t j = lane; j < n; j += 32) {
+                const uint32_t key = staged_keys[sm.wlist[warp][j] - lo];
+                gt += key > prefix ? 1u : 0u;
+                eq += key == prefix ? 1u : 0u;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                gt += __shfl_xor_sync(0xffffffffu, gt, off);
+                eq += __shfl_xor_sync(0xffffffffu, eq, off);
+            }
+            if (lane == 0) {
+                sm.warp_sum[warp] = gt;
+                sm.warp_sum2[warp] = eq;
+            }
+        }
+        __syncthreads();
+        uint32_t n_out = out_off, n_eq = eq_before;
+        for (int w = 0; w < warp; ++w) {
+            const uint32_t eqw = sm.warp_sum2[w];
+            n_out += sm.warp_sum[w] + (n_eq >= need ? 0u : min(eqw, need - n_eq));
+            n_eq += eqw;
+        }
+        for (uint32_t j0 = 0; j0 < n; j0 += 32) {
+            const uint32_t j = j0 + lane;
+            int32_t e = 0;
+            uint32_t key = 0;
+            if (j < n) {
+                e = sm.wlist[warp][j];
+                key = staged_keys[e - lo];
+            }
+            const bool is_gt = j < n && key > prefix, is_eq = j < n && key == prefix;
+            const uint32_t bal_eq = __ballot_sync(0xffffffffu, is_eq);
+            const uint32_t eq_rank = n_eq + __popc(bal_eq & lt);
+            const bool pick = is_gt || (is_eq && eq_rank < need);
+            const uint32_t bal_pick = __ballot_sync(0xffffffffu, pick);
+            if (pick) {
+                const uint32_t pos = n_out + __popc(bal_pick & lt);
+                if (pos < (uint32_t)p.k) {
+                    sel_out[pos] = e;
+                    if (pos - out_off < (uint32_t)kTopkPickCap) sm.pick_pos[pos - out_off] = e;
+                } else {
+                    raise_status(0x10u);
+                }
+            }
+            n_out += __popc(bal_pick);
+            n_eq += __popc(bal_eq);
+        }
     } else {
-        const int wspan = (((hi - lo) + kTopkWarps - 1) / kTopkWarps + 127) & ~127;
-        const int wlo = min(hi, lo + warp * wspan), whi = min(hi, wlo + wspan);
         {
             uint32_t gt = 0, eq = 0;
             for (int e = wlo + 4 * lane; e < whi; e += 128) {
@@ -386,7 +493,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
             n_out += sm.warp_sum[w] + (n_eq >= need ? 0u : min(eqw, need - n_eq));
             n_eq += eqw;
         }
-        const uint32_t lt = (1u << lane) - 1u;
         for (int e0 = wlo; e0 < whi; e0 += 128) {
             const int e = e0 + 4 * lane;
             uint32_t gt_bits = 0, eq_bits = 0;
@@ -444,7 +550,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
 
     // Gather this CTA's rows [out_off, out_off + cta_picks) into the compact pool: first every
     // row's pool row (from the slice's block-table entries), then all copies, 16 bytes per thread
-    // per unit, twelve units in flight per thread.
+    // per unit, six units in flight per thread.
     const size_t seq_row0 = (size_t)b * p.npk * kSparsePage;
     const uint32_t n_rows = min(cta_picks, (uint32_t)p.k - min(out_off, (uint32_t)p.k));
     auto resolve = [&](uint32_t i) -> int {  // pool row of this CTA's i-th pick, or -1
@@ -460,7 +566,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
     __syncthreads();
     tr.at(0x8233);
     constexpr int kUnits = kSparseRow / 8;  // 16-byte pieces of a row
-    constexpr int kGatherU = 12;
+    constexpr int kGatherU = 6;
     const uint4 *pool4 = reinterpret_cast<const uint4 *>(p.kv_pool);
     uint4 *out4 = reinterpret_cast<uint4 *>(p.sel_pool) + (seq_row0 + out_off) * kUnits;
     const uint32_t n_units = n_rows * kUnits;

@@ -132,6 +132,23 @@ def test_topk_ties_nan_inf_and_signed_zeros(seed):
         _check_selection(s.numpy(), case.seq_lens.numpy(), k, si, sn, sbt, sp, pool, bt)
 
 
+@pytest.mark.parametrize("k", [1, 1000, 30000])
+def test_topk_long_tie_heavy_slices(k):
+    """70000 integer scores: every warp's share of the candidates overflows its list, so the
+    kernel takes its full-scan path; and one sequence of distinct scores beside it."""
+    g = torch.Generator().manual_seed(k)
+    lens = [70000, 70000]
+    max_pages = (max(lens) + 63) // 64
+    s = torch.randint(-3, 4, (2, max_pages * 64), generator=g).float()
+    s[1] = torch.randn(max_pages * 64, generator=g)
+    case = workloads.make_case("t", lens, shuffle=True, q_mode="none", seed=k)
+    pool, bt, sl = case.pool.to(DEV), case.block_table.to(DEV), case.seq_lens.to(DEV)
+    si, sp, sbt, sn = mla.topk_gather(s.to(DEV), sl, pool, bt, k)
+    torch.cuda.synchronize()
+    _check_selection(s.numpy(), case.seq_lens.numpy(), k, si, sn, sbt, sp, pool, bt)
+    assert mla.get_device_status() == (0, 0)
+
+
 def test_selection_agrees_with_the_oracles_own_scores_up_to_near_ties():
     sc = workloads.make_sparse_case("s", [30000, 12000], k=300, shuffle=True, seed=5)
     d = _to_dev(sc)
