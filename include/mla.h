@@ -305,7 +305,8 @@ size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k);
  * where S_b = the selected positions.  q_abs [batch, 1, 128, 576] bf16; sel_index
  * [batch, k] int32 receives the selection when not NULL.  Other arguments as above
  * and as mla_decode; workspace of at least mla_decode_sparse_workspace_size() bytes,
- * 16-byte aligned, not shared by overlapping calls.  Five kernels are enqueued.
+ * 16-byte aligned, not shared by overlapping calls.  Five kernels are enqueued.  A selection of
+ * at most 16 pages per sequence (k <= 1024) is decoded without splitting a sequence.
  */
 mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
                                const int32_t *block_table, const int32_t *seq_lens, int batch, int n_heads,

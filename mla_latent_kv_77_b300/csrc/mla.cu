@@ -284,6 +284,7 @@ mla_status_t launch_error(uint64_t kernels = 1) {
 }
 
 constexpr int kMaxTopK = 1 << 18;
+constexpr int kSparseWholePages = 16;  // selections up to this many pages per sequence are not split
 
 // Workspace of the indexer decode: scores, selection, compact pool and its table, then the
 // decode's own workspace.
@@ -295,7 +296,8 @@ bool sparse_ws_layout(int batch, int max_pages, int k, SparseWs *w) {
     if (batch < 1 || batch > kMaxRows || max_pages < 1 || k < 1 || k > kMaxTopK) return false;
     if ((long long)max_pages * kPage > 0x7fffffffll) return false;
     w->npk = (k + kPage - 1) / kPage;
-    const size_t dec = mla_decode_workspace_size(batch, 1, 0);
+    const size_t dec0 = mla_decode_workspace_size(batch, 1, 0), dec1 = mla_decode_workspace_size(batch, 1, 1);
+    const size_t dec = dec0 > dec1 ? dec0 : dec1;
     if (dec == 0) return false;
     size_t off = 0;
     w->scores = off;
@@ -859,7 +861,10 @@ mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void 
     st = mla_topk_gather(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool,
                          sel_bt, sel_lens, stream);
     if (st != MLA_OK) return st;
-    return mla_decode(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, n_heads, batch * w.npk, w.npk, scale, 0, 0,
+    // a selection of at most 16 pages per sequence is decoded whole, one item per sequence: split
+    // into pieces, each piece's fp32 partial epilogue and the merge cost more than its pages
+    const int splits = w.npk <= kSparseWholePages ? 1 : 0;
+    return mla_decode(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, n_heads, batch * w.npk, w.npk, scale, 0, splits,
                       o_lat, lse, ws + w.dec, w.dec_bytes, stream);
 }
 
