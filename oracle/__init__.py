@@ -79,6 +79,12 @@ def _load():
         lib.oracle_topk_row.argtypes = [_f64p, ctypes.c_long, ctypes.c_long,
                                         np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")]
         lib.oracle_topk_row.restype = ctypes.c_long
+        _u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_index_scores_e4m3.argtypes = [_f32p, _u8p, _f32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_long, _f64p]
+        lib.oracle_index_scores_e4m3.restype = None
         for fn in ("oracle_absorb_q", "oracle_up_proj", "oracle_decode_absorbed", "oracle_decode_naive",
                    "oracle_combine", "oracle_rope", "oracle_cache_append", "oracle_compress",
                    "oracle_cache_append_compressed", "oracle_index_scores"):
@@ -322,3 +328,26 @@ def decode_sparse(q_abs, q_idx, pool, idx_pool, block_table, seq_lens, k: int, s
         comp.reshape(B, n_pages * page, D)[b, :rows[b].shape[0]] = rows[b]
     o, lse = decode_absorbed(q, comp, cbt, lens, scale, causal=False, d_c=d_c)
     return o, lse, sel
+
+
+def e4m3_value(code: int) -> float:
+    """The value of one FP8 E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+    subnormals at exponent 0, S.1111.111 NaN, no infinity)."""
+    return float(_load().oracle_e4m3_value(int(code) & 0xFF))
+
+
+def index_scores_e4m3(q_idx, idx_codes, idx_scale, block_table, seq_lens, max_len: int | None = None) -> np.ndarray:
+    """s[b, t] = scale(b, t) * q_idx[b] . value(codes(b, t)) for t < seq_lens[b] (NaN elsewhere).
+    idx_codes [P, page, d_idx] uint8 (E4M3 codes), idx_scale [P, page] float32."""
+    q = _f32(q_idx)
+    codes = np.ascontiguousarray(np.asarray(idx_codes.cpu() if hasattr(idx_codes, "cpu") else idx_codes,
+                                            dtype=np.uint8))
+    sc = _f32(idx_scale)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    B, d_idx = q.shape
+    page = codes.shape[1]
+    if max_len is None:
+        max_len = int(sl.max()) if sl.size else 0
+    out = np.full((B, max(1, max_len)), np.nan, dtype=np.float64)
+    _load().oracle_index_scores_e4m3(q, codes, sc, bt, sl, B, d_idx, page, bt.shape[1], max(1, max_len), out)
+    return out[:, :max_len]

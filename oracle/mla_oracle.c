@@ -578,3 +578,38 @@ long oracle_topk_row(const double *s, long n, long k, long *out) {
     qsort(out, (size_t)take, sizeof(long), cmp_long);
     return take;
 }
+
+/*
+ * The value of one FP8 E4M3 code (the OCP 8-bit floating-point format's E4M3 variant, as used
+ * for low-bit caches): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field
+ * 0 holds the subnormals m/8 * 2^-6; S.1111.111 is NaN and there is no infinity, so
+ * S.1111.110 = 448 is the largest magnitude.
+ */
+double oracle_e4m3_value(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 0xF, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * Index scores over an e4m3 index cache with one scale per cached token (the indexer of the
+ * DeepSeek page's "KV cache data movement minimization" section, with its index vectors held
+ * in 8 bits): s[b][t] = scale(b, t) * sum_d q_idx[b][d] * value(code(b, t, d)), where
+ * code(b, t, :) = idx_codes[block_table[b, t / page], t % page, :] and scale(b, t) is the
+ * scale array's entry at the same place.  Entries t >= seq_lens[b] are left untouched.
+ */
+void oracle_index_scores_e4m3(const float *q_idx, const uint8_t *idx_codes, const float *idx_scale,
+                              const int32_t *block_table, const int32_t *seq_lens, int B, int d_idx, int page,
+                              int max_pages, long max_len, double *scores) {
+    for (int b = 0; b < B; ++b) {
+        const long L = seq_lens[b];
+        for (long t = 0; t < L && t < max_len; ++t) {
+            const size_t slot = (size_t)block_table[(size_t)b * max_pages + t / page] * page + t % page;
+            const uint8_t *k = idx_codes + slot * d_idx;
+            double acc = 0.0;
+            for (int d = 0; d < d_idx; ++d) acc += (double)q_idx[(size_t)b * d_idx + d] * oracle_e4m3_value(k[d]);
+            scores[(size_t)b * max_len + t] = (double)idx_scale[slot] * acc;
+        }
+    }
+}

@@ -152,3 +152,68 @@ def test_sparse_decode_of_an_empty_sequence_is_empty():
     o, lse, sel = oracle.decode_sparse(q, qi, pool, ipool, bt, sl, 3, 0.3, d_c=32)
     assert sel[0].size == 0 and np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
     assert sel[1].size == 3
+
+
+# ---------------------------------------------------------------------------------------------
+# E4M3 index cache (index vectors held in 8 bits with one scale per token)
+# ---------------------------------------------------------------------------------------------
+
+def test_e4m3_values_from_the_format_definition():
+    """Hand-computed codes: sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals at
+    exponent 0, S.1111.111 the only NaN, no infinity."""
+    cases = {0x00: 0.0, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0xC0: -2.0, 0x7E: 448.0, 0xFE: -448.0,
+             0x08: 2.0 ** -6, 0x07: 7 / 8 * 2.0 ** -6, 0x01: 2.0 ** -9, 0x30: 0.5, 0x77: 240.0, 0x7F: None,
+             0xFF: None}
+    for code, want in cases.items():
+        got = oracle.e4m3_value(code)
+        if want is None:
+            assert math.isnan(got), hex(code)
+        else:
+            assert got == want, (hex(code), got, want)
+    assert math.copysign(1.0, oracle.e4m3_value(0x80)) == -1.0
+
+
+def test_e4m3_values_match_an_independent_conversion():
+    """Every one of the 256 codes against torch's float8_e4m3fn conversion (written elsewhere)."""
+    import torch
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3_value(c) for c in range(256)])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got[~both_nan], ref[~both_nan].astype(np.float64))
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+
+
+def test_e4m3_codes_are_monotone_in_magnitude():
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+
+
+def test_e4m3_index_scores_are_scaled_dot_products():
+    rng = _rng(40)
+    lens = [30, 3, 0]
+    P, page, d = 8, 16, 8
+    codes = rng.integers(0, 256, (P, page, d), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A  # no NaN codes
+    scale = rng.uniform(0.01, 2.0, (P, page)).astype(np.float32)
+    bt = rng.permutation(P).astype(np.int32)[:6].reshape(3, 2)
+    q = rng.standard_normal((3, d)).astype(np.float32)
+    s = oracle.index_scores_e4m3(q, codes, scale, bt, np.array(lens, np.int32))
+    for b, L in enumerate(lens):
+        for t in range(L):
+            pg, sl = bt[b, t // page], t % page
+            want = float(scale[pg, sl]) * sum(float(q[b, i]) * oracle.e4m3_value(codes[pg, sl, i]) for i in range(d))
+            assert abs(s[b, t] - want) <= 1e-12 * (1 + abs(want))
+
+
+def test_e4m3_index_scores_equal_the_bf16_scores_of_the_decoded_vectors():
+    """Decoding the codes, multiplying by the scales and scoring as a float index cache gives the
+    same numbers (scale 1 and e4m3 values are exact in float32)."""
+    rng = _rng(41)
+    codes = rng.integers(0, 0x7E, (4, 16, 32), dtype=np.uint8)
+    table = np.array([oracle.e4m3_value(c) for c in range(256)], dtype=np.float32)
+    bt = np.arange(4, dtype=np.int32).reshape(2, 2)
+    sl = np.array([32, 20], np.int32)
+    q = rng.standard_normal((2, 32)).astype(np.float32)
+    a = oracle.index_scores_e4m3(q, codes, np.ones((4, 16), np.float32), bt, sl)
+    b = oracle.index_scores(q, table[codes], bt, sl)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
