@@ -511,7 +511,8 @@ def sparse_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_index: int 
     (five launches and their argument checks) comes close to the device time, so the calls
     issued back to back between one event pair are also reported, as `us_issued`.  Each of its
     two own kernels alone is replayed the same way (the index scores alternating between the two
-    index caches).  Roofline of the call:
+    index caches).  The whole call is also timed over the E4M3 form of the index cache (codes and
+    one scale per token: d_idx + 4 bytes per token instead of 2 d_idx), as `e4m3_index`.  Roofline of the call:
     the index vectors it must read plus the selected rows; of the score kernel: the index vectors."""
     import torch
     name = "sparse_b8_l128k_k512"
@@ -553,8 +554,18 @@ def sparse_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_index: int 
     topk_us = graph_us([lambda st: mla.lib().mla_topk_gather(
         mla._ptr(scores), mla._ptr(sl), mla._ptr(pools[0]), mla._ptr(bt), c.B, c.num_pages, c.max_pages, sc.k,
         mla._ptr(sel[0]), mla._ptr(sel[1]), mla._ptr(sel[2]), mla._ptr(sel[3]), mla._stream(st))], steps)
+    # the same call over the E4M3 form of the index cache (codes and one scale per token)
+    sc8 = workloads.make_sparse_workload(name, seed=0, device=dev, e4m3=True)
+    codes = [sc8.idx_codes, sc8.idx_codes.clone()]
+    scl = [sc8.idx_scale, sc8.idx_scale.clone()]
+    us8 = graph_us([lambda st, k=k: mla.decode_sparse(c.q_abs, sc8.q_idx, pools[k], codes[k], bt, sl, sc.k, c.scale,
+                                                      o_lat=o, lse=l, sel_index=si, workspace=ws, stream=st,
+                                                      idx_scale=scl[k]) for k in range(2)], max(1, steps // 2))
+    score8_us = graph_us([lambda st, k=k: mla.index_scores_e4m3(sc8.q_idx, codes[k], scl[k], bt, sl, scores=scores,
+                                                                stream=st) for k in range(2)], max(1, steps // 2))
     st_, word = mla.get_device_status()
     assert st_ == 0, f"device status {word:#x}"
+    idx8_bytes = sc8.index_bytes(e4m3=True)
     idx_bytes, sel_bytes = sc.index_bytes(), sc.selected_bytes()
     call_bytes = idx_bytes + sel_bytes
     res = {"workload": name, "batch": c.B, "context": int(c.seq_lens.max()), "k": sc.k, "d_idx": sc.d_idx,
@@ -563,10 +574,15 @@ def sparse_leg(mla, workloads, dev, steps: int, warmup: int, pk, gpu_index: int 
            "index_scores": {"us": score_us, "bytes": idx_bytes, "achieved_gbs": idx_bytes / (score_us * 1e-6) / 1e9,
                             "frac": idx_bytes / (score_us * 1e-6) / 1e9 / pk["hbm_gbs"]},
            "topk_gather_us": topk_us,
+           "e4m3_index": {"us": us8, "tokens_per_s": c.B / (us8 * 1e-6),
+                          "call_roofline_frac": (idx8_bytes + sel_bytes) / (pk["hbm_gbs"] * 1e9) / (us8 * 1e-6),
+                          "index_scores": {"us": score8_us, "bytes": idx8_bytes,
+                                           "achieved_gbs": idx8_bytes / (score8_us * 1e-6) / 1e9,
+                                           "frac": idx8_bytes / (score8_us * 1e-6) / 1e9 / pk["hbm_gbs"]}},
            "timing": "CUDA-graph replays alternating two caches (the whole call and each kernel alone); "
                      "us_issued: K calls issued back to back from Python between one event pair",
            "clocks": clk.summary()}
-    del sc, c, pools, idxs, ws, scores, sel
+    del sc, c, pools, idxs, ws, scores, sel, sc8, codes, scl
     torch.cuda.empty_cache()
     return res
 

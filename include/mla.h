@@ -263,6 +263,20 @@ mla_status_t mla_index_scores(const void *q_idx, const void *idx_pool, const int
                               float *scores, mla_stream_t stream);
 
 /*
+ * mla_index_scores_e4m3 - the same scores over an index cache held in 8 bits: every index
+ * vector is d_idx FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * subnormals at exponent 0, S.1111.111 NaN, no infinity) and one float32 scale per token:
+ *     scores[b, t] = idx_scale[p, t % 64] * sum_d q_idx[b, d] * value(idx_codes[p, t % 64, d]),
+ *     p = block_table[b, t / 64]
+ * (each product and the sum in fp32, then the scale).  Half the index bytes of the bf16 form.
+ * idx_codes [num_pages, 64, d_idx] uint8, 16-byte aligned; idx_scale [num_pages, 64] float32.
+ * Other arguments, limits and device-side checks as mla_index_scores.
+ */
+mla_status_t mla_index_scores_e4m3(const void *q_idx, const void *idx_codes, const float *idx_scale,
+                                   const int32_t *block_table, const int32_t *seq_lens, int batch, int d_idx,
+                                   int num_pages, int max_pages, float *scores, mla_stream_t stream);
+
+/*
  * mla_topk_gather - the k best tokens of each sequence and their cache rows.
  * Sequence b selects the min(k, L_b) positions with the largest scores[b, t],
  * t < L_b; equal scores go to the lower position first, and a NaN score ranks
@@ -303,16 +317,18 @@ size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k);
  *     o_lat[b, 0, h] = sum_{t in S_b} softmax_t(scale * q_abs[b, 0, h] . row_t) row_t[0:512]
  *     lse[b, 0, h]   = log sum_{t in S_b} exp(scale * q_abs[b, 0, h] . row_t)
  * where S_b = the selected positions.  q_abs [batch, 1, 128, 576] bf16; sel_index
- * [batch, k] int32 receives the selection when not NULL.  Other arguments as above
+ * [batch, k] int32 receives the selection when not NULL.  idx_scale NULL: idx_pool is the bf16
+ * index cache of mla_index_scores; otherwise idx_pool holds E4M3 codes and idx_scale their
+ * per-token scales, as mla_index_scores_e4m3.  Other arguments as above
  * and as mla_decode; workspace of at least mla_decode_sparse_workspace_size() bytes,
  * 16-byte aligned, not shared by overlapping calls.  Five kernels are enqueued.  A selection of
  * at most 16 pages per sequence (k <= 1024) is decoded without splitting a sequence.
  */
 mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
-                               const int32_t *block_table, const int32_t *seq_lens, int batch, int n_heads,
-                               int d_idx, int num_pages, int max_pages, int k, float scale, void *o_lat,
-                               float *lse, int32_t *sel_index, void *workspace, size_t workspace_bytes,
-                               mla_stream_t stream);
+                               const float *idx_scale, const int32_t *block_table, const int32_t *seq_lens,
+                               int batch, int n_heads, int d_idx, int num_pages, int max_pages, int k, float scale,
+                               void *o_lat, float *lse, int32_t *sel_index, void *workspace,
+                               size_t workspace_bytes, mla_stream_t stream);
 
 /*
  * mla_get_device_status - synchronise `stream`, then read and clear the

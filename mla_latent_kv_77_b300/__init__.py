@@ -69,10 +69,11 @@ EXPORTS = {
     "mla_cache_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _VP]),
     "mla_cache_append_compressed": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP]),
     "mla_index_scores": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
+    "mla_index_scores_e4m3": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     "mla_topk_gather": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
     "mla_decode_sparse_workspace_size": (_SZ, [_I, _I, _I]),
-    "mla_decode_sparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _VP, _SZ,
-                               _VP]),
+    "mla_decode_sparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _VP,
+                               _SZ, _VP]),
     "mla_get_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "mla_cache_bytes": (ctypes.c_uint64, [ctypes.c_int64, _I, _I, _I, _I]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
@@ -298,6 +299,28 @@ def index_scores(q_idx, idx_pool, block_table, seq_lens, scores=None, stream=Non
     return scores
 
 
+def index_scores_e4m3(q_idx, idx_codes, idx_scale, block_table, seq_lens, scores=None, stream=None):
+    """Index scores over an E4M3 index cache: scores[b, t] = scale(b, t) * q_idx[b] . value(codes(b, t)).
+    idx_codes [P, 64, d_idx] uint8 (or float8_e4m3fn), idx_scale [P, 64] f32.  Returns [B, max_pages * 64] f32."""
+    import torch
+    _need(q_idx, torch.bfloat16, "q_idx")
+    if idx_codes.dtype != torch.uint8:
+        idx_codes = idx_codes.view(torch.uint8)
+    _need(idx_codes, torch.uint8, "idx_codes")
+    _need(idx_scale, torch.float32, "idx_scale")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, d_idx = q_idx.shape
+    max_pages = block_table.shape[1]
+    if scores is None:
+        scores = torch.empty(B, max_pages * PAGE, dtype=torch.float32, device=q_idx.device)
+    _need(scores, torch.float32, "scores")
+    _check(lib().mla_index_scores_e4m3(_ptr(q_idx), _ptr(idx_codes), _ptr(idx_scale), _ptr(block_table),
+                                       _ptr(seq_lens), B, d_idx, idx_codes.shape[0], max_pages, _ptr(scores),
+                                       _stream(stream)), "mla_index_scores_e4m3")
+    return scores
+
+
 def topk_gather(scores, seq_lens, kv_pool, block_table, k: int, stream=None):
     """The k best-scored tokens of each sequence (ties: lower position; NaN last) and their cache rows.
 
@@ -326,15 +349,22 @@ def decode_sparse_workspace_size(batch: int, max_pages: int, k: int) -> int:
 
 
 def decode_sparse(q_abs, q_idx, kv_pool, idx_pool, block_table, seq_lens, k: int, scale: float = SCALE,
-                  o_lat=None, lse=None, sel_index=None, workspace=None, stream=None) -> Tuple:
+                  o_lat=None, lse=None, sel_index=None, workspace=None, stream=None, idx_scale=None) -> Tuple:
     """The indexer decode of one new token per sequence: index scores, top k, the decode over the k
-    selected tokens.  q_abs [B, 1, 128, 576] bf16, q_idx [B, d_idx] bf16, idx_pool [P, 64, d_idx] bf16.
+    selected tokens.  q_abs [B, 1, 128, 576] bf16, q_idx [B, d_idx] bf16, idx_pool [P, 64, d_idx] bf16
+    (or, with idx_scale [P, 64] f32, E4M3 codes as uint8 / float8_e4m3fn).
     Returns (o_lat [B, 1, 128, 512] bf16, lse [B, 1, 128] f32, sel_index [B, k] int32)."""
     import torch
     _need(q_abs, torch.bfloat16, "q_abs")
     _need(q_idx, torch.bfloat16, "q_idx")
     _need(kv_pool, torch.bfloat16, "kv_pool")
-    _need(idx_pool, torch.bfloat16, "idx_pool")
+    if idx_scale is None:
+        _need(idx_pool, torch.bfloat16, "idx_pool")
+    else:
+        if idx_pool.dtype != torch.uint8:
+            idx_pool = idx_pool.view(torch.uint8)
+        _need(idx_pool, torch.uint8, "idx_pool")
+        _need(idx_scale, torch.float32, "idx_scale")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Tq, nh, _ = q_abs.shape
@@ -354,7 +384,8 @@ def decode_sparse(q_abs, q_idx, kv_pool, idx_pool, block_table, seq_lens, k: int
     if workspace is None:
         workspace = torch.empty(max(1, decode_sparse_workspace_size(B, max_pages, int(k))), dtype=torch.uint8,
                                 device=dev)
-    st = lib().mla_decode_sparse(_ptr(q_abs), _ptr(q_idx), _ptr(kv_pool), _ptr(idx_pool), _ptr(block_table),
+    st = lib().mla_decode_sparse(_ptr(q_abs), _ptr(q_idx), _ptr(kv_pool), _ptr(idx_pool),
+                                 _ptr(idx_scale) if idx_scale is not None else None, _ptr(block_table),
                                  _ptr(seq_lens), B, nh, q_idx.shape[1], kv_pool.shape[0], max_pages, int(k),
                                  float(scale), _ptr(o_lat), _ptr(lse), _ptr(sel_index), _ptr(workspace),
                                  workspace.numel(), _stream(stream))

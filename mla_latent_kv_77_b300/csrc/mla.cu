@@ -316,6 +316,59 @@ bool sparse_ws_layout(int batch, int max_pages, int k, SparseWs *w) {
     return true;
 }
 
+// The index-score launch for a bf16 index cache, or E4M3 codes with per-token scales.
+mla_status_t index_scores_impl(const void *q_idx, const void *idx_pool, const float *idx_scale, bool e4m3,
+                               const int32_t *block_table, const int32_t *seq_lens, int batch, int d_idx,
+                               int num_pages, int max_pages, float *scores, mla_stream_t stream) {
+    if (!q_idx || !idx_pool || !block_table || !seq_lens || !scores) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || num_pages < 1 || max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (d_idx != 32 && d_idx != 64 && d_idx != 128 && d_idx != 256) return MLA_ERR_SHAPE;
+    if (batch > kMaxRows || (long long)max_pages * kPage > 0x7fffffffll ||
+        (long long)num_pages * kPage * d_idx > (1ll << 40))
+        return MLA_ERR_SHAPE;
+    if (!aligned16(q_idx) || !aligned16(idx_pool) || !aligned4(scores) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || (e4m3 && !aligned4(idx_scale)))
+        return MLA_ERR_ALIGNMENT;
+    int dev;
+    DeviceInfo *info;
+    mla_status_t st = device_setup(&dev, &info);
+    if (st != MLA_OK) return st;
+    // about 32 warps per SM over the whole batch, each taking a few pages of one sequence
+    const long long warps = (long long)info->sms * 32;
+    const long long pages = (long long)batch * max_pages;
+    const long long per_warp = pages <= warps ? 1 : (pages + warps - 1) / warps;
+    const int wpc = kScoreThreads / 32;
+    const int cps = (int)((max_pages + wpc * per_warp - 1) / (wpc * per_warp));
+    ScoreParams p;
+    p.q_idx = static_cast<const __nv_bfloat16 *>(q_idx);
+    p.idx_pool = idx_pool;
+    p.idx_scale = idx_scale;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.scores = scores;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.ctas_per_seq = cps;
+    const dim3 grid((unsigned)((long long)batch * cps));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (e4m3) {
+        switch (d_idx) {
+            case 32: index_score_kernel<2, true><<<grid, kScoreThreads, 0, s>>>(p); break;
+            case 64: index_score_kernel<4, true><<<grid, kScoreThreads, 0, s>>>(p); break;
+            case 128: index_score_kernel<8, true><<<grid, kScoreThreads, 0, s>>>(p); break;
+            default: index_score_kernel<16, true><<<grid, kScoreThreads, 0, s>>>(p); break;
+        }
+    } else {
+        switch (d_idx) {
+            case 32: index_score_kernel<4, false><<<grid, kScoreThreads, 0, s>>>(p); break;
+            case 64: index_score_kernel<8, false><<<grid, kScoreThreads, 0, s>>>(p); break;
+            case 128: index_score_kernel<16, false><<<grid, kScoreThreads, 0, s>>>(p); break;
+            default: index_score_kernel<32, false><<<grid, kScoreThreads, 0, s>>>(p); break;
+        }
+    }
+    return launch_error();
+}
+
 // Device address of the library-owned decode scratch on each device, looked up once.
 void *g_scratch_addr[kMaxDevices] = {};
 
@@ -733,43 +786,16 @@ mla_status_t mla_combine(const float *o_parts, const float *lse_parts, int n_par
 mla_status_t mla_index_scores(const void *q_idx, const void *idx_pool, const int32_t *block_table,
                               const int32_t *seq_lens, int batch, int d_idx, int num_pages, int max_pages,
                               float *scores, mla_stream_t stream) {
-    if (!q_idx || !idx_pool || !block_table || !seq_lens || !scores) return MLA_ERR_INVALID_ARG;
-    if (batch < 1 || num_pages < 1 || max_pages < 1) return MLA_ERR_INVALID_ARG;
-    if (d_idx != 32 && d_idx != 64 && d_idx != 128 && d_idx != 256) return MLA_ERR_SHAPE;
-    if (batch > kMaxRows || (long long)max_pages * kPage > 0x7fffffffll ||
-        (long long)num_pages * kPage * d_idx > (1ll << 40))
-        return MLA_ERR_SHAPE;
-    if (!aligned16(q_idx) || !aligned16(idx_pool) || !aligned4(scores) || !aligned4(block_table) ||
-        !aligned4(seq_lens))
-        return MLA_ERR_ALIGNMENT;
-    int dev;
-    DeviceInfo *info;
-    mla_status_t st = device_setup(&dev, &info);
-    if (st != MLA_OK) return st;
-    // about 32 warps per SM over the whole batch, each taking a few pages of one sequence
-    const long long warps = (long long)info->sms * 32;
-    const long long pages = (long long)batch * max_pages;
-    const long long per_warp = pages <= warps ? 1 : (pages + warps - 1) / warps;
-    const int wpc = kScoreThreads / 32;
-    const int cps = (int)((max_pages + wpc * per_warp - 1) / (wpc * per_warp));
-    ScoreParams p;
-    p.q_idx = static_cast<const __nv_bfloat16 *>(q_idx);
-    p.idx_pool = static_cast<const __nv_bfloat16 *>(idx_pool);
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.scores = scores;
-    p.num_pages = num_pages;
-    p.max_pages = max_pages;
-    p.ctas_per_seq = cps;
-    const dim3 grid((unsigned)((long long)batch * cps));
-    cudaStream_t s = (cudaStream_t)stream;
-    switch (d_idx) {
-        case 32: index_score_kernel<4><<<grid, kScoreThreads, 0, s>>>(p); break;
-        case 64: index_score_kernel<8><<<grid, kScoreThreads, 0, s>>>(p); break;
-        case 128: index_score_kernel<16><<<grid, kScoreThreads, 0, s>>>(p); break;
-        default: index_score_kernel<32><<<grid, kScoreThreads, 0, s>>>(p); break;
-    }
-    return launch_error();
+    return index_scores_impl(q_idx, idx_pool, nullptr, false, block_table, seq_lens, batch, d_idx, num_pages,
+                             max_pages, scores, stream);
+}
+
+mla_status_t mla_index_scores_e4m3(const void *q_idx, const void *idx_codes, const float *idx_scale,
+                                   const int32_t *block_table, const int32_t *seq_lens, int batch, int d_idx,
+                                   int num_pages, int max_pages, float *scores, mla_stream_t stream) {
+    if (!idx_scale) return MLA_ERR_INVALID_ARG;
+    return index_scores_impl(q_idx, idx_codes, idx_scale, true, block_table, seq_lens, batch, d_idx, num_pages,
+                             max_pages, scores, stream);
 }
 
 mla_status_t mla_topk_gather(const float *scores, const int32_t *seq_lens, const void *kv_pool,
@@ -832,10 +858,10 @@ size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k) {
 }
 
 mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
-                               const int32_t *block_table, const int32_t *seq_lens, int batch, int n_heads,
-                               int d_idx, int num_pages, int max_pages, int k, float scale, void *o_lat,
-                               float *lse, int32_t *sel_index, void *workspace, size_t workspace_bytes,
-                               mla_stream_t stream) {
+                               const float *idx_scale, const int32_t *block_table, const int32_t *seq_lens,
+                               int batch, int n_heads, int d_idx, int num_pages, int max_pages, int k, float scale,
+                               void *o_lat, float *lse, int32_t *sel_index, void *workspace,
+                               size_t workspace_bytes, mla_stream_t stream) {
     if (!q_abs || !q_idx || !kv_pool || !idx_pool || !block_table || !seq_lens || !o_lat || !lse)
         return MLA_ERR_INVALID_ARG;
     if (batch < 1 || num_pages < 1 || max_pages < 1 || k < 1) return MLA_ERR_INVALID_ARG;
@@ -855,8 +881,8 @@ mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void 
     void *sel_pool = ws + w.sel_pool;
     int32_t *sel_bt = reinterpret_cast<int32_t *>(ws + w.sel_bt);
     int32_t *sel_lens = reinterpret_cast<int32_t *>(ws + w.sel_lens);
-    mla_status_t st = mla_index_scores(q_idx, idx_pool, block_table, seq_lens, batch, d_idx, num_pages, max_pages,
-                                       scores, stream);
+    mla_status_t st = index_scores_impl(q_idx, idx_pool, idx_scale, idx_scale != nullptr, block_table, seq_lens,
+                                        batch, d_idx, num_pages, max_pages, scores, stream);
     if (st != MLA_OK) return st;
     st = mla_topk_gather(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool,
                          sel_bt, sel_lens, stream);

@@ -3,10 +3,11 @@
 // all of them with one dot product each, keeps the k best, and attends over those tokens only.
 //
 //   index_score_kernel   s[b, t] = q_idx[b] . k_idx(b, t) for every cached token t < L_b: a
-//                        stream over the paged index cache (d_idx bf16 per token), fp32 sums.
-//                        It moves d_idx * 2 bytes per token and does d_idx multiply-adds, so it
-//                        runs at HBM speed: consecutive lanes read consecutive 16-byte pieces of
-//                        the same page, eight loads in flight per lane.
+//                        stream over the paged index cache (d_idx bf16 per token, or d_idx E4M3
+//                        codes and one fp32 scale per token), fp32 sums.  It moves d_idx * 2 (or
+//                        d_idx + 4) bytes per token and does d_idx multiply-adds, so it runs at
+//                        HBM speed: consecutive lanes read consecutive 16-byte pieces of the same
+//                        page, eight loads in flight per lane.
 //   topk_gather_kernel   the k largest scores of each sequence (ties: the lower index; NaN
 //                        below every number), by a radix select over the scores' order-keeping
 //                        32-bit keys, one byte per pass, on a cluster of CTAs that each own a
@@ -18,6 +19,8 @@
 //                        against L_b rows of index vectors read to find them.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -68,18 +71,29 @@ __device__ __forceinline__ int sparse_len(const int32_t *seq_lens, int b, int ca
 // ---------------------------------------------------------------------------------------------
 struct ScoreParams {
     const __nv_bfloat16 *q_idx;     // [B, d_idx]
-    const __nv_bfloat16 *idx_pool;  // [num_pages, 64, d_idx]
+    const void *idx_pool;           // [num_pages, 64, d_idx] bf16, or E4M3 codes
+    const float *idx_scale;         // [num_pages, 64]: per-token scales of E4M3 codes
     const int32_t *block_table;     // [B, max_pages]
     const int32_t *seq_lens;        // [B]
     float *scores;                  // [B, max_pages * 64]
     int num_pages, max_pages, ctas_per_seq;
 };
 
-template <int LPT>
+// Two E4M3 codes (low byte first) as two floats; the conversion is exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair & 0xFFFFu), __NV_E4M3);
+    return __half22float2(__half2(h));
+}
+
+// E4M3 = false: bf16 index vectors, 8 per 16-byte piece.  E4M3 = true: 16 codes per piece, and the
+// token's dot product is multiplied by its scale.
+template <int LPT, bool E4M3>
 __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams p) {
+    constexpr int kPer = E4M3 ? 16 : 8;                // index coordinates per lane piece
     constexpr int kTokPerLoad = 32 / LPT;
     constexpr int kLoadsPerPage = kSparsePage / kTokPerLoad;
-    constexpr int kDIdx = LPT * 8;
+    constexpr int kU = kLoadsPerPage < kScoreUnroll ? kLoadsPerPage : kScoreUnroll;
+    constexpr int kDIdx = LPT * kPer;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = blockIdx.x / p.ctas_per_seq, c = blockIdx.x % p.ctas_per_seq;
     const long long row_len = (long long)p.max_pages * kSparsePage;
@@ -87,14 +101,15 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
     const int n_pages = (L + kSparsePage - 1) / kSparsePage;
     const int sub = lane % LPT, tok = lane / LPT;
 
-    float q[8];
-    {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p.q_idx + (size_t)b * kDIdx + sub * 8);
+    float q[kPer];
+#pragma unroll
+    for (int h = 0; h < kPer / 8; ++h) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p.q_idx + (size_t)b * kDIdx + sub * kPer + h * 8);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            q[2 * i] = bf16lo_to_f32(w[i]);
-            q[2 * i + 1] = bf16hi_to_f32(w[i]);
+            q[h * 8 + 2 * i] = bf16lo_to_f32(w[i]);
+            q[h * 8 + 2 * i + 1] = bf16hi_to_f32(w[i]);
         }
     }
     float *out = p.scores + (size_t)b * row_len;
@@ -107,34 +122,61 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
             for (int i = lane; i < kSparsePage && base + i < L; i += 32) out[base + i] = __int_as_float(0x7FC00000);
             continue;
         }
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.idx_pool + (size_t)pg * kSparsePage * kDIdx) + lane;
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.idx_pool) +
+                                                           (size_t)pg * kSparsePage * kDIdx * (E4M3 ? 1 : 2)) +
+                           lane;
+        // the page's 64 token scales, two per lane, loaded beside the codes
+        float sc_lo = 1.f, sc_hi = 1.f;
+        if constexpr (E4M3) {
+            sc_lo = __ldg(p.idx_scale + (size_t)pg * kSparsePage + lane);
+            sc_hi = __ldg(p.idx_scale + (size_t)pg * kSparsePage + 32 + lane);
+        }
 #pragma unroll
-        for (int g = 0; g < kLoadsPerPage; g += kScoreUnroll) {
-            uint4 v[kScoreUnroll];
+        for (int g = 0; g < kLoadsPerPage; g += kU) {
+            uint4 v[kU];
 #pragma unroll
-            for (int u = 0; u < kScoreUnroll; ++u) v[u] = __ldcs(src + (g + u) * 32);
-            float s[kScoreUnroll];
+            for (int u = 0; u < kU; ++u) v[u] = __ldcs(src + (g + u) * 32);
+            float s[kU];
 #pragma unroll
-            for (int u = 0; u < kScoreUnroll; ++u) {
+            for (int u = 0; u < kU; ++u) {
                 const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
                 float a = 0.f;
+                if constexpr (E4M3) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    a = fmaf(q[2 * i], bf16lo_to_f32(w[i]), a);
-                    a = fmaf(q[2 * i + 1], bf16hi_to_f32(w[i]), a);
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f0 = e4m3x2_to_float2(w[i]), f1 = e4m3x2_to_float2(w[i] >> 16);
+                        a = fmaf(q[4 * i], f0.x, a);
+                        a = fmaf(q[4 * i + 1], f0.y, a);
+                        a = fmaf(q[4 * i + 2], f1.x, a);
+                        a = fmaf(q[4 * i + 3], f1.y, a);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a = fmaf(q[2 * i], bf16lo_to_f32(w[i]), a);
+                        a = fmaf(q[2 * i + 1], bf16hi_to_f32(w[i]), a);
+                    }
                 }
                 s[u] = a;
             }
 #pragma unroll
             for (int off = LPT / 2; off > 0; off >>= 1) {
 #pragma unroll
-                for (int u = 0; u < kScoreUnroll; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+                for (int u = 0; u < kU; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+            }
+            if constexpr (E4M3) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = (g + u) * kTokPerLoad + tok;  // token within the page
+                    const float a = __shfl_sync(0xffffffffu, sc_lo, i & 31), b2 = __shfl_sync(0xffffffffu, sc_hi, i & 31);
+                    s[u] *= i < 32 ? a : b2;
+                }
             }
             if (sub == 0) {
 #pragma unroll
-                for (int u = 0; u < kScoreUnroll; ++u) {
-                    const int t = base + (g + u) * kTokPerLoad + tok;
-                    if (t < L) out[t] = s[u];
+                for (int u = 0; u < kU; ++u) {
+                    const int i = (g + u) * kTokPerLoad + tok;  // token within the page
+                    if (base + i < L) out[base + i] = s[u];
                 }
             }
         }

@@ -27,6 +27,9 @@ reproducible on its own; the ragged lengths come first, from a generator seeded
        pool row; with ``ties`` set, instead integers uniform in [-2, 2] (many exactly equal
        scores, to exercise the tie rule)
   k=14 q_idx        ~ N(0, 1), bf16 (with ``ties``: integers uniform in [-2, 2])
+  --   the E4M3 form of the index cache (no draw): each token's scale is its largest
+       |coordinate| / 448 (float32), its codes the coordinates divided by the scale, converted
+       by torch's float8_e4m3fn (round to nearest even)
 
 Shapes follow the DeepSeek-V2 attention: 128 heads, 512-d latent, 64-d decoupled
 RoPE key, 128-d head, 576-number cache row, 64-token pages.
@@ -310,14 +313,18 @@ class SparseCase:
     idx_pool: torch.Tensor          # [num_pages, PAGE, d_idx] bf16
     q_idx: torch.Tensor             # [B, d_idx] bf16
     k: int
+    idx_codes: Optional[torch.Tensor] = None  # [num_pages, PAGE, d_idx] uint8 (E4M3 codes)
+    idx_scale: Optional[torch.Tensor] = None  # [num_pages, PAGE] float32
 
     @property
     def d_idx(self) -> int:
         return int(self.idx_pool.shape[2])
 
-    def index_bytes(self) -> int:
-        """Bytes of index cache one step reads (each visible token's vector once)."""
-        return int(self.case.seq_lens.to(torch.int64).sum()) * self.d_idx * 2
+    def index_bytes(self, e4m3: bool = False) -> int:
+        """Bytes of index cache one step reads (each visible token's vector once; in E4M3, its
+        codes and its scale)."""
+        per = self.d_idx + 4 if e4m3 else self.d_idx * 2
+        return int(self.case.seq_lens.to(torch.int64).sum()) * per
 
     def selected_bytes(self) -> int:
         """Bytes of latent cache rows the selection gathers: min(k, L_b) rows per sequence."""
@@ -326,7 +333,7 @@ class SparseCase:
 
 def make_sparse_case(name: str, seq_lens: List[int], k: int, d_idx: int = D_IDX, ties: bool = False,
                      shuffle: bool = False, spare_pages: int = 0, garbage: Optional[str] = None,
-                     peaked_frac: float = 0.0, seed: int = 0, device="cpu") -> SparseCase:
+                     peaked_frac: float = 0.0, e4m3: bool = False, seed: int = 0, device="cpu") -> SparseCase:
     case = make_case(name, seq_lens, Tq=1, causal=False, shuffle=shuffle, spare_pages=spare_pages,
                      garbage=garbage, peaked_frac=peaked_frac, q_mode="abs", seed=seed, device=device)
     shape = (case.num_pages, PAGE, d_idx)
@@ -337,7 +344,13 @@ def make_sparse_case(name: str, seq_lens: List[int], k: int, d_idx: int = D_IDX,
     else:
         idx = _randn_bf16(shape, 1.0 / math.sqrt(d_idx), seed, 13, device)
         q_idx = _randn_bf16((case.B, d_idx), 1.0, seed, 14, device)
-    return SparseCase(case=case, idx_pool=idx, q_idx=q_idx, k=int(k))
+    sc = SparseCase(case=case, idx_pool=idx, q_idx=q_idx, k=int(k))
+    if e4m3:
+        v = idx.float()
+        scale = (v.abs().amax(dim=2) / 448.0).clamp_min(2.0 ** -100)
+        sc.idx_codes = (v / scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        sc.idx_scale = scale.contiguous()
+    return sc
 
 
 # Indexer decode workloads: the 128K-token batch with the page's top-k of 512.
@@ -348,5 +361,5 @@ SPARSE_WORKLOADS = {
 }
 
 
-def make_sparse_workload(name: str, seed: int = 0, device="cpu") -> SparseCase:
-    return make_sparse_case(name, seed=seed, device=device, **SPARSE_WORKLOADS[name])
+def make_sparse_workload(name: str, seed: int = 0, device="cpu", e4m3: bool = False) -> SparseCase:
+    return make_sparse_case(name, seed=seed, device=device, e4m3=e4m3, **SPARSE_WORKLOADS[name])

@@ -186,6 +186,14 @@ def test_indexer_calls_reject_bad_arguments_on_host(lib):
     assert scores(pool=40) == mla.Status.ALIGNMENT
     assert scores(sc=66) == mla.Status.ALIGNMENT
 
+    def scores8(d_idx=128, codes=32, scale=64):
+        return lib.mla_index_scores_e4m3(vp(16), vp(codes), vp(scale) if scale else None, vp(48), vp(80), 2, d_idx,
+                                         4, 2, vp(96), None)
+    assert scores8(scale=None) == mla.Status.INVALID_ARG
+    assert scores8(d_idx=48) == mla.Status.SHAPE
+    assert scores8(codes=40) == mla.Status.ALIGNMENT
+    assert scores8(scale=66) == mla.Status.ALIGNMENT
+
     def topk(k=512, B=2, sc=16, pool=32, sp=48, si=64):
         return lib.mla_topk_gather(vp(sc), vp(80), vp(pool), vp(96), B, 4, 2, k, vp(si) if si else None, vp(sp),
                                    vp(112), vp(128), None)
@@ -206,8 +214,8 @@ def test_indexer_calls_reject_bad_arguments_on_host(lib):
 
     def sparse(k=512, nh=128, d_idx=128, ws=256, nbytes=None, scale=0.07, qa=16):
         nb = need if nbytes is None else nbytes
-        return lib.mla_decode_sparse(vp(qa), vp(32), vp(48), vp(64), vp(80), vp(96), 8, nh, d_idx, 4096, 2048, k,
-                                     scale, vp(112), vp(128), None, vp(ws) if ws else None, nb, None)
+        return lib.mla_decode_sparse(vp(qa), vp(32), vp(48), vp(64), None, vp(80), vp(96), 8, nh, d_idx, 4096, 2048,
+                                     k, scale, vp(112), vp(128), None, vp(ws) if ws else None, nb, None)
     assert sparse(ws=None) == mla.Status.WORKSPACE
     assert sparse(nbytes=need - 1) == mla.Status.WORKSPACE
     assert sparse(nh=64) == mla.Status.UNSUPPORTED

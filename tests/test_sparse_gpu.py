@@ -255,6 +255,67 @@ def test_decode_sparse_with_k_above_every_length_is_the_dense_decode():
         assert np.array_equal(sel[b, :L], np.arange(L)) and np.all(sel[b, L:] == -1)
 
 
+def _check_scores_e4m3(sc, got):
+    """Each score within (d_idx + 1) * 2^-24 * scale * sum |q_i v_i| of the oracle's: the products
+    of a bf16 coordinate and an E4M3 value are exact in fp32, the sum and the scale round."""
+    c = sc.case
+    codes, scale = sc.idx_codes.cpu().numpy(), sc.idx_scale.cpu().numpy()
+    ref = oracle.index_scores_e4m3(_np(sc.q_idx), codes, scale, c.block_table.numpy(), c.seq_lens.numpy())
+    table = np.array([oracle.e4m3_value(x) for x in range(256)])
+    absv = np.abs(table[codes]) * scale[..., None]
+    q = np.abs(_np(sc.q_idx))
+    g = got.cpu().numpy().astype(np.float64)
+    bt = c.block_table.numpy()
+    for b in range(c.B):
+        L = int(c.seq_lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        mag = absv[bt[b, t // 64], t % 64] @ q[b]
+        bound = (sc.d_idx + 1) * 2.0 ** -24 * mag + 1e-30
+        err = np.abs(g[b, :L] - ref[b, :L])
+        assert np.all(err <= bound), (b, float((err / bound).max()))
+    return ref
+
+
+@pytest.mark.parametrize("d_idx", [32, 64, 128, 256])
+def test_index_scores_e4m3_match_oracle(d_idx):
+    sc = workloads.make_sparse_case("s", [1, 63, 64, 65, 700, 0, 1500], k=8, d_idx=d_idx, shuffle=True,
+                                    spare_pages=3, e4m3=True, seed=50 + d_idx)
+    d = _to_dev(sc)
+    codes, scale = sc.idx_codes.to(DEV), sc.idx_scale.to(DEV)
+    sentinel = torch.full((sc.case.B, sc.case.max_pages * 64), 12345.0, device=DEV)
+    got = mla.index_scores_e4m3(d["q_idx"], codes, scale, d["bt"], d["sl"], scores=sentinel)
+    torch.cuda.synchronize()
+    _check_scores_e4m3(sc, got)
+    for b in range(sc.case.B):
+        assert torch.all(got[b, int(sc.case.seq_lens[b]):] == 12345.0)
+    assert mla.get_device_status() == (0, 0)
+
+
+def test_decode_sparse_with_an_e4m3_index_cache():
+    k = 300
+    sc = workloads.make_sparse_case("s", [0, 40, 700, 5000, 20000], k=k, shuffle=True, spare_pages=2, garbage="nan",
+                                    e4m3=True, seed=60)
+    d = _to_dev(sc)
+    codes, scale = sc.idx_codes.to(DEV), sc.idx_scale.to(DEV)
+    o, lse, si = mla.decode_sparse(d["q_abs"], d["q_idx"], d["pool"], codes, d["bt"], d["sl"], k, idx_scale=scale)
+    torch.cuda.synchronize()
+    assert mla.get_device_status() == (0, 0)
+    scores = mla.index_scores_e4m3(d["q_idx"], codes, scale, d["bt"], d["sl"])
+    _check_scores_e4m3(sc, scores)
+    s_np = scores.cpu().numpy()
+    sel = si.cpu().numpy()
+    lens = np.minimum(sc.case.seq_lens.numpy(), k)
+    for b in range(sc.case.B):
+        L = int(sc.case.seq_lens[b])
+        want = oracle.topk_row(s_np[b, :L].astype(np.float64), k) if L else np.zeros(0)
+        assert np.array_equal(sel[b, :lens[b]], want)
+    o_ref, l_ref, extra = _oracle_over_selection(sc, sel, lens, range(sc.case.B))
+    _check_sparse_out(o, o_ref, extra)
+    check_lse(lse, l_ref)
+
+
 def test_bad_block_table_and_length_are_reported_not_faulted():
     sc = workloads.make_sparse_case("s", [200, 100], k=16, seed=4)
     d = _to_dev(sc)
