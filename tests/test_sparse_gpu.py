@@ -149,6 +149,44 @@ def test_topk_long_tie_heavy_slices(k):
     assert mla.get_device_status() == (0, 0)
 
 
+@pytest.mark.parametrize("k", [1, 700, 5000])
+def test_topk_past_the_shared_memory_copy(k):
+    """409600 positions: each CTA's slice (51200) is longer than the shared-memory key copy holds,
+    so every pass reads the scores from global memory.  The block table aliases 8 physical pages
+    (reads only), and a second sequence of integer scores (ties) rides along."""
+    g = torch.Generator().manual_seed(100 + k)
+    max_pages = 6400
+    lens = [max_pages * 64, 300000]
+    s = torch.randn(2, max_pages * 64, generator=g)
+    s[1] = torch.randint(-3, 4, (max_pages * 64,), generator=g).float()
+    pool = workloads._randn_bf16((8, 64, workloads.D), 0.5, k, 1, DEV)
+    bt = (torch.arange(max_pages, dtype=torch.int32) % 8).repeat(2, 1).contiguous()
+    sl = torch.tensor(lens, dtype=torch.int32)
+    si, sp, sbt, sn = mla.topk_gather(s.to(DEV), sl.to(DEV), pool, bt.to(DEV), k)
+    torch.cuda.synchronize()
+    _check_selection(s.numpy(), lens, k, si, sn, sbt, sp, pool, bt.to(DEV))
+    assert mla.get_device_status() == (0, 0)
+
+
+def test_sparse_decode_many_clusters():
+    """64 sequences: 512 top-k CTAs run in several waves; checked on four of them."""
+    k = 100
+    lens = [2000 + 37 * i for i in range(64)]
+    sc = workloads.make_sparse_case("s", lens, k=k, shuffle=True, seed=70)
+    d = _to_dev(sc)
+    o, lse, si = mla.decode_sparse(d["q_abs"], d["q_idx"], d["pool"], d["idx"], d["bt"], d["sl"], k)
+    scores = mla.index_scores(d["q_idx"], d["idx"], d["bt"], d["sl"])
+    torch.cuda.synchronize()
+    assert mla.get_device_status() == (0, 0)
+    s_np, sel = scores.cpu().numpy(), si.cpu().numpy()
+    for b in range(64):
+        assert np.array_equal(sel[b], oracle.topk_row(s_np[b, :lens[b]].astype(np.float64), k)), b
+    seqs = [0, 21, 42, 63]
+    o_ref, l_ref, extra = _oracle_over_selection(sc, sel, np.full(64, k), seqs)
+    _check_sparse_out(o[seqs], o_ref, extra)
+    check_lse(lse[seqs], l_ref)
+
+
 def test_selection_agrees_with_the_oracles_own_scores_up_to_near_ties():
     sc = workloads.make_sparse_case("s", [30000, 12000], k=300, shuffle=True, seed=5)
     d = _to_dev(sc)
