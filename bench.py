@@ -54,15 +54,17 @@ def peaks():
 
 def kernel_source_hash() -> str:
     """Hash of what the decode launch is built from: the decode kernels, the PTX wrappers they
-    use, and mla_decode's launch code in mla.cu (the rest of mla.cu serves other calls)."""
+    use, and the decode's launch code in mla.cu (decode_enqueue and mla_decode; the rest of
+    mla.cu serves other calls)."""
     csrc = os.path.join(ROOT, "mla_latent_kv_77_b300", "csrc")
     h = hashlib.sha256()
     for f in ("decode_kernels.cuh", "ptx.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     host = open(os.path.join(csrc, "mla.cu"), "rb").read()
-    a = host.find(b"mla_status_t mla_decode(")
-    b = host.find(b"mla_status_t mla_decode_static_scratch(")
-    h.update(host[a:b] if 0 <= a < b else host)
+    for start, end in ((b"mla_status_t decode_enqueue(", b"// (end of the decode launch code)"),
+                       (b"mla_status_t mla_decode(", b"mla_status_t mla_decode_static_scratch(")):
+        a, b = host.find(start), host.find(end)
+        h.update(host[a:b] if 0 <= a < b else host)
     return h.hexdigest()[:16]
 
 

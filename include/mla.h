@@ -321,8 +321,9 @@ size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k);
  * index cache of mla_index_scores; otherwise idx_pool holds E4M3 codes and idx_scale their
  * per-token scales, as mla_index_scores_e4m3.  Other arguments as above
  * and as mla_decode; workspace of at least mla_decode_sparse_workspace_size() bytes,
- * 16-byte aligned, not shared by overlapping calls.  Five kernels are enqueued.  A selection of
- * at most 16 pages per sequence (k <= 1024) is decoded without splitting a sequence.
+ * 16-byte aligned, not shared by overlapping calls.  A selection of at most 16 pages per
+ * sequence (k <= 1024) is decoded without splitting a sequence, and the top-k kernel writes that
+ * decode plan itself: four kernels are enqueued (five for larger k).
  */
 mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void *kv_pool, const void *idx_pool,
                                const float *idx_scale, const int32_t *block_table, const int32_t *seq_lens,

@@ -369,6 +369,155 @@ mla_status_t index_scores_impl(const void *q_idx, const void *idx_pool, const fl
     return launch_error();
 }
 
+// The decode launch: the split plan (unless the caller's kernel already wrote it into the
+// workspace: one item per query), the decode, the LSE combine.  Arguments already checked.
+mla_status_t decode_enqueue(const void *q_abs, const void *kv_pool, const int32_t *block_table,
+                            const int32_t *seq_lens, int batch, int q_len, int num_pages, int max_pages, float scale,
+                            int causal, int num_splits, void *o_lat, float *lse, uint8_t *ws, const WsLayout &w,
+                            int dev, const DeviceInfo *info, bool run_plan, cudaStream_t s) {
+    // pages: all 9 column blocks (score stage) or the 8 latent blocks (value stage) of one page;
+    // queries: 4 content blocks of all 128 heads, or the RoPE block of 64 heads
+    const uint64_t pool_rows = (uint64_t)num_pages * kPage, q_rows = (uint64_t)batch * q_len * kHeads;
+    CUtensorMap tmap_s, tmap_v, tmap_qc, tmap_qr;
+    if (!map_cached(&tmap_s, dev, kv_pool, pool_rows, kPage, kBoxesS) ||
+        !map_cached(&tmap_v, dev, kv_pool, pool_rows, kPage, kBoxesV) ||
+        !map_cached(&tmap_qc, dev, q_abs, q_rows, kHeads, 4) || !map_cached(&tmap_qr, dev, q_abs, q_rows, 64, 1))
+        return MLA_ERR_CUDA;
+
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + w.hdr);
+    Item *items = reinterpret_cast<Item *>(ws + w.items);
+    BtInfo *bt_info = reinterpret_cast<BtInfo *>(ws + w.info);
+    const int n_bt = batch * q_len;
+
+    if (run_plan) {
+        // one thread per query up to kPlanThreads (the rank sort wants that), in whole warps, at
+        // least four: a small batch plans with few threads and few warps to synchronise
+        const int plan_threads = n_bt >= kPlanThreads ? kPlanThreads : (n_bt <= 128 ? 128 : (n_bt + 31) / 32 * 32);
+        // a programmatic dependent of whatever precedes it (it waits for that to complete before
+        // reading anything): its launch overlaps the previous call's combine kernel
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(1, 1, 1);
+        pcfg.blockDim = dim3((unsigned)plan_threads, 1, 1);
+        pcfg.stream = s;
+        cudaLaunchAttribute pat[1];
+        pat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pat[0].val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = pat;
+        pcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&pcfg, plan_kernel, seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
+                               num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch),
+                               w.max_items, w.max_slots) != cudaSuccess) {
+            cudaGetLastError();
+            return MLA_ERR_CUDA;
+        }
+    }
+
+    DecodeParams p;
+    p.q_abs = static_cast<const __nv_bfloat16 *>(q_abs);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.o_lat = static_cast<__nv_bfloat16 *>(o_lat);
+    p.lse = lse;
+    p.hdr = hdr;
+    p.items = items;
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+    p.ring = ws + w.ring;
+    p.B = batch;
+    p.Tq = q_len;
+    p.causal = causal ? 1 : 0;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.max_items = w.max_items;
+    p.sl2 = scale * 1.4426950408889634f;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * info->clusters, 1, 1);
+    cfg.blockDim = dim3(kDecodeThreads, 1, 1);
+    cfg.dynamicSmemBytes = kDecodeSmem;
+    cfg.stream = s;
+    // the decode and combine kernels are programmatic dependents of their predecessors: their
+    // launch and prologue overlap the predecessor, and they wait for its results on the device
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, tmap_qc, tmap_qr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    cudaLaunchConfig_t ccfg = {};
+    const int units = n_bt * (kHeads / kCombineHeads);
+    ccfg.gridDim = dim3(units < 2 * info->sms ? units : 2 * info->sms, 1, 1);
+    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
+    ccfg.stream = s;
+    ccfg.attrs = &at[1];
+    ccfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&ccfg, combine_kernel, (const PlanHeader *)hdr, (const BtInfo *)bt_info, (const float *)p.part_o,
+                           (const float *)p.part_lse, p.o_lat, lse) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    g_launches += run_plan ? 3 : 2;  // plan, decode, combine
+    return MLA_OK;
+}
+// (end of the decode launch code)
+
+// The top-k launch (arguments already checked).  plan_ws != null: the kernel also writes the
+// decode plan of its output into that decode workspace (layout w): one whole item per sequence.
+mla_status_t topk_enqueue(const float *scores, const int32_t *seq_lens, const void *kv_pool,
+                          const int32_t *block_table, int batch, int num_pages, int max_pages, int k,
+                          int32_t *sel_index, void *sel_pool, int32_t *sel_block_table, int32_t *sel_lens,
+                          uint8_t *plan_ws, int plan_max_items, int plan_max_slots, cudaStream_t s,
+                          const WsLayout *w = nullptr) {
+    TopkParams p;
+    p.scores = scores;
+    p.seq_lens = seq_lens;
+    p.kv_pool = static_cast<const __nv_bfloat16 *>(kv_pool);
+    p.block_table = block_table;
+    p.sel_index = sel_index;
+    p.sel_pool = static_cast<__nv_bfloat16 *>(sel_pool);
+    p.sel_block_table = sel_block_table;
+    p.sel_lens = sel_lens;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.k = k;
+    p.npk = (k + kPage - 1) / kPage;
+    p.plan_hdr = plan_ws && w ? reinterpret_cast<PlanHeader *>(plan_ws + w->hdr) : nullptr;
+    p.plan_items = plan_ws && w ? reinterpret_cast<Item *>(plan_ws + w->items) : nullptr;
+    p.plan_info = plan_ws && w ? reinterpret_cast<BtInfo *>(plan_ws + w->info) : nullptr;
+    p.plan_max_items = plan_max_items;
+    p.plan_max_slots = plan_max_slots;
+    // the largest slice any CTA can own (a sequence of max_pages * 64 tokens): staged in shared
+    // memory when it fits
+    const long long max_chunk = (((long long)max_pages * kPage + kTopkCluster - 1) / kTopkCluster + 3) & ~3ll;
+    p.staged = max_chunk <= kTopkStageKeys ? 1 : 0;
+    const size_t dyn = p.staged ? (size_t)max_chunk * sizeof(uint32_t) : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(batch * kTopkCluster), 1, 1);
+    cfg.blockDim = dim3(kTopkThreads, 1, 1);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kTopkCluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_gather_kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    g_launches += 1;
+    return MLA_OK;
+}
+
 // Device address of the library-owned decode scratch on each device, looked up once.
 void *g_scratch_addr[kMaxDevices] = {};
 
@@ -644,98 +793,9 @@ mla_status_t mla_decode(const void *q_abs, const void *kv_pool, const int32_t *b
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
 
-    // pages: all 9 column blocks (score stage) or the 8 latent blocks (value stage) of one page;
-    // queries: 4 content blocks of all 128 heads, or the RoPE block of 64 heads
-    const uint64_t pool_rows = (uint64_t)num_pages * kPage, q_rows = (uint64_t)batch * q_len * kHeads;
-    CUtensorMap tmap_s, tmap_v, tmap_qc, tmap_qr;
-    if (!map_cached(&tmap_s, dev, kv_pool, pool_rows, kPage, kBoxesS) ||
-        !map_cached(&tmap_v, dev, kv_pool, pool_rows, kPage, kBoxesV) ||
-        !map_cached(&tmap_qc, dev, q_abs, q_rows, kHeads, 4) || !map_cached(&tmap_qr, dev, q_abs, q_rows, 64, 1))
-        return MLA_ERR_CUDA;
-
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + w.hdr);
-    Item *items = reinterpret_cast<Item *>(ws + w.items);
-    BtInfo *bt_info = reinterpret_cast<BtInfo *>(ws + w.info);
-    const int n_bt = batch * q_len;
-    cudaStream_t s = (cudaStream_t)stream;
-
-    // one thread per query up to kPlanThreads (the rank sort wants that), in whole warps, at
-    // least four: a small batch plans with few threads and few warps to synchronise
-    const int plan_threads = n_bt >= kPlanThreads ? kPlanThreads : (n_bt <= 128 ? 128 : (n_bt + 31) / 32 * 32);
-    {
-        // a programmatic dependent of whatever precedes it (it waits for that to complete before
-        // reading anything): its launch overlaps the previous call's combine kernel
-        cudaLaunchConfig_t pcfg = {};
-        pcfg.gridDim = dim3(1, 1, 1);
-        pcfg.blockDim = dim3((unsigned)plan_threads, 1, 1);
-        pcfg.stream = s;
-        cudaLaunchAttribute pat[1];
-        pat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        pat[0].val.programmaticStreamSerializationAllowed = 1;
-        pcfg.attrs = pat;
-        pcfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&pcfg, plan_kernel, seq_lens, batch, q_len, causal ? 1 : 0, max_pages, info->clusters,
-                               num_splits, hdr, items, bt_info, reinterpret_cast<int *>(ws + w.scratch), w.max_items,
-                               w.max_slots) != cudaSuccess) {
-            cudaGetLastError();
-            return MLA_ERR_CUDA;
-        }
-    }
-
-    DecodeParams p;
-    p.q_abs = static_cast<const __nv_bfloat16 *>(q_abs);
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.o_lat = static_cast<__nv_bfloat16 *>(o_lat);
-    p.lse = lse;
-    p.hdr = hdr;
-    p.items = items;
-    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
-    p.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
-    p.ring = ws + w.ring;
-    p.B = batch;
-    p.Tq = q_len;
-    p.causal = causal ? 1 : 0;
-    p.num_pages = num_pages;
-    p.max_pages = max_pages;
-    p.max_items = w.max_items;
-    p.sl2 = scale * 1.4426950408889634f;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * info->clusters, 1, 1);
-    cfg.blockDim = dim3(kDecodeThreads, 1, 1);
-    cfg.dynamicSmemBytes = kDecodeSmem;
-    cfg.stream = s;
-    // the decode and combine kernels are programmatic dependents of their predecessors: their
-    // launch and prologue overlap the predecessor, and they wait for its results on the device
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, decode_kernel, tmap_s, tmap_v, tmap_qc, tmap_qr, p) != cudaSuccess) {
-        cudaGetLastError();
-        return MLA_ERR_CUDA;
-    }
-    cudaLaunchConfig_t ccfg = {};
-    const int units = n_bt * (kHeads / kCombineHeads);
-    ccfg.gridDim = dim3(units < 2 * info->sms ? units : 2 * info->sms, 1, 1);
-    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
-    ccfg.stream = s;
-    ccfg.attrs = &at[1];
-    ccfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&ccfg, combine_kernel, (const PlanHeader *)hdr, (const BtInfo *)bt_info, (const float *)p.part_o,
-                           (const float *)p.part_lse, p.o_lat, lse) != cudaSuccess) {
-        cudaGetLastError();
-        return MLA_ERR_CUDA;
-    }
-    g_launches += 3;  // plan, decode, combine
-    return MLA_OK;
+    return decode_enqueue(q_abs, kv_pool, block_table, seq_lens, batch, q_len, num_pages, max_pages, scale, causal,
+                          num_splits, o_lat, lse, static_cast<uint8_t *>(workspace), w, dev, info, true,
+                          (cudaStream_t)stream);
 }
 
 mla_status_t mla_decode_static_scratch(const void *q_abs, const void *kv_pool, const int32_t *block_table,
@@ -813,42 +873,8 @@ mla_status_t mla_topk_gather(const float *scores, const int32_t *seq_lens, const
     DeviceInfo *info;
     mla_status_t st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
-    TopkParams p;
-    p.scores = scores;
-    p.seq_lens = seq_lens;
-    p.kv_pool = static_cast<const __nv_bfloat16 *>(kv_pool);
-    p.block_table = block_table;
-    p.sel_index = sel_index;
-    p.sel_pool = static_cast<__nv_bfloat16 *>(sel_pool);
-    p.sel_block_table = sel_block_table;
-    p.sel_lens = sel_lens;
-    p.num_pages = num_pages;
-    p.max_pages = max_pages;
-    p.k = k;
-    p.npk = (k + kPage - 1) / kPage;
-    // the largest slice any CTA can own (a sequence of max_pages * 64 tokens): staged in shared
-    // memory when it fits
-    const long long max_chunk = (((long long)max_pages * kPage + kTopkCluster - 1) / kTopkCluster + 3) & ~3ll;
-    p.staged = max_chunk <= kTopkStageKeys ? 1 : 0;
-    const size_t dyn = p.staged ? (size_t)max_chunk * sizeof(uint32_t) : 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(batch * kTopkCluster), 1, 1);
-    cfg.blockDim = dim3(kTopkThreads, 1, 1);
-    cfg.dynamicSmemBytes = dyn;
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kTopkCluster;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_gather_kernel, p) != cudaSuccess) {
-        cudaGetLastError();
-        return MLA_ERR_CUDA;
-    }
-    g_launches += 1;
-    return MLA_OK;
+    return topk_enqueue(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel_index, sel_pool,
+                        sel_block_table, sel_lens, nullptr, 0, 0, (cudaStream_t)stream);
 }
 
 size_t mla_decode_sparse_workspace_size(int batch, int max_pages, int k) {
@@ -884,14 +910,29 @@ mla_status_t mla_decode_sparse(const void *q_abs, const void *q_idx, const void 
     mla_status_t st = index_scores_impl(q_idx, idx_pool, idx_scale, idx_scale != nullptr, block_table, seq_lens,
                                         batch, d_idx, num_pages, max_pages, scores, stream);
     if (st != MLA_OK) return st;
-    st = mla_topk_gather(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool,
-                         sel_bt, sel_lens, stream);
+    // A selection of at most 16 pages per sequence is decoded whole, one item per sequence (split
+    // into pieces, each piece's fp32 partial epilogue and the merge cost more than its pages).
+    // That plan is written by the top-k kernel itself, so the decode needs no plan launch.
+    const bool whole = w.npk <= kSparseWholePages;
+    if (!whole) {
+        st = mla_topk_gather(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool,
+                             sel_bt, sel_lens, stream);
+        if (st != MLA_OK) return st;
+        return mla_decode(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, n_heads, batch * w.npk, w.npk, scale, 0, 0,
+                          o_lat, lse, ws + w.dec, w.dec_bytes, stream);
+    }
+    int dev;
+    DeviceInfo *info;
+    st = device_setup(&dev, &info);
     if (st != MLA_OK) return st;
-    // a selection of at most 16 pages per sequence is decoded whole, one item per sequence: split
-    // into pieces, each piece's fp32 partial epilogue and the merge cost more than its pages
-    const int splits = w.npk <= kSparseWholePages ? 1 : 0;
-    return mla_decode(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, n_heads, batch * w.npk, w.npk, scale, 0, splits,
-                      o_lat, lse, ws + w.dec, w.dec_bytes, stream);
+    WsLayout dl;
+    if (!ws_layout(batch, 1, 1, &dl) || dl.total > w.dec_bytes) return MLA_ERR_SHAPE;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = topk_enqueue(scores, seq_lens, kv_pool, block_table, batch, num_pages, max_pages, k, sel, sel_pool, sel_bt,
+                      sel_lens, ws + w.dec, dl.max_items, dl.max_slots, s, &dl);
+    if (st != MLA_OK) return st;
+    return decode_enqueue(q_abs, sel_pool, sel_bt, sel_lens, batch, 1, batch * w.npk, w.npk, scale, 0, 1, o_lat, lse,
+                          ws + w.dec, dl, dev, info, false, s);
 }
 
 mla_status_t mla_test_bounded_wait(int limit_ms, mla_stream_t stream) {

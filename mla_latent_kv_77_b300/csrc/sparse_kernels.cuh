@@ -23,6 +23,7 @@
 #include <cuda_fp8.h>
 #include <cstdint>
 
+#include "decode_kernels.cuh"
 #include "ptx.cuh"
 
 namespace mla {
@@ -198,6 +199,12 @@ struct TopkParams {
     int32_t *sel_lens;              // [B]: min(k, L_b)
     int num_pages, max_pages, k, npk;
     int staged;                     // 1: each CTA first copies its slice's keys into shared memory
+    // optional: the decode plan of the output (one whole item per sequence), in the decode
+    // workspace, so the decode that follows needs no plan launch
+    PlanHeader *plan_hdr;
+    Item *plan_items;
+    BtInfo *plan_info;
+    int plan_max_items, plan_max_slots;
 };
 
 // Slice positions that fit the staged key copy (dynamic shared memory next to TopkSmem).
@@ -643,7 +650,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
     }
     if (r == 0) {
         for (int j = tid; j < p.npk; j += kTopkThreads) p.sel_block_table[(size_t)b * p.npk + j] = b * p.npk + j;
-        if (tid == 0) p.sel_lens[b] = sel_len;
+        if (tid == 0) {
+            p.sel_lens[b] = sel_len;
+            if (p.plan_items != nullptr) {
+                // the plan the decode's planner makes for one unsplit query per sequence (the
+                // item order only changes which CTA pair takes which item)
+                const int tiles = (sel_len + kSparsePage - 1) / kSparsePage;
+                Item it;
+                it.bt = b, it.tb = 0, it.te = tiles, it.slot = -1, it.b = b, it.n_vis = sel_len;
+                it.pad0 = it.pad1 = 0;
+                p.plan_items[b] = it;
+                BtInfo in;
+                in.splits = 1, in.slot_base = -1, in.tiles = tiles, in.item_off = b;
+                p.plan_info[b] = in;
+                if (b == 0) {
+                    p.plan_hdr->n_items = (int)(gridDim.x / kTopkCluster);
+                    p.plan_hdr->n_bt = (int)(gridDim.x / kTopkCluster);
+                    p.plan_hdr->n_split = 0;
+                    p.plan_hdr->max_items = p.plan_max_items;
+                    p.plan_hdr->max_slots = p.plan_max_slots;
+                }
+            }
+        }
     }
     // no CTA leaves while another may still read its histograms
     if (!take_all) cluster_wait();
