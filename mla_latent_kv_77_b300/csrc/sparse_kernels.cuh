@@ -12,7 +12,10 @@
 //                        below every number), by a radix select over the scores' order-keeping
 //                        32-bit keys, one byte per pass, on a cluster of CTAs that each own a
 //                        contiguous slice of the sequence and add their 256-bin histograms
-//                        through distributed shared memory.  The same kernel writes the selected
+//                        through distributed shared memory; after the second pass each warp
+//                        keeps the few positions that can still be picked in an ordered list, and
+//                        the later passes and the compaction read only those.  The same kernel
+//                        writes the selected
 //                        positions in ascending order and copies the selected cache rows into a
 //                        compact page pool, which the dense decode then walks (its lengths and an
 //                        identity block table included): the gather costs k rows of traffic,
@@ -66,9 +69,10 @@ __device__ __forceinline__ int sparse_len(const int32_t *seq_lens, int b, int ca
 }
 
 // ---------------------------------------------------------------------------------------------
-// Index scores.  LPT = lanes per token = d_idx / 8: each lane holds 8 query coordinates and reads
-// the same 8 coordinates of 32 / LPT tokens per 512-byte warp load.  A CTA of 8 warps takes pages
-// j = c * 8 + w (and every ctas_per_seq * 8 pages after) of sequence b = blockIdx.x / ctas_per_seq.
+// Index scores.  LPT = lanes per token = d_idx / 8 (bf16) or d_idx / 16 (E4M3): each lane holds
+// the 8 or 16 query coordinates of its 16-byte piece of a token and reads those coordinates of
+// 32 / LPT tokens per 512-byte warp load.  A CTA of 8 warps takes pages j = c * 8 + w (and every
+// ctas_per_seq * 8 pages after) of sequence b = blockIdx.x / ctas_per_seq.
 // ---------------------------------------------------------------------------------------------
 struct ScoreParams {
     const __nv_bfloat16 *q_idx;     // [B, d_idx]
