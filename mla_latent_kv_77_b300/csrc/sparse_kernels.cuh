@@ -39,7 +39,8 @@ constexpr int kTopkCluster = 8;          // CTAs per sequence (portable cluster 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkBins = 256;           // one byte of the key per pass
-constexpr int kTopkPickCap = 1024;   // picks per CTA whose positions are kept in shared memory
+constexpr int kTopkPickCap = 512;    // picks per CTA whose positions are kept in shared memory
+constexpr int kTopkCandCap = 64;     // keys per CTA offered to the cluster after the second pass
 constexpr int kTopkListCap = 128;    // positions per warp list (keys at or above the first pass's bin)
 
 // Order-keeping key of an fp32 score: larger score, larger key.  -0 is +0 (they tie), every NaN
@@ -228,6 +229,11 @@ struct TopkSmem {
                                               // least the first pass's chosen byte, in order
     uint32_t wlist_n[kTopkWarps];
     uint32_t list_overflow;
+    uint32_t cand[kTopkCandCap];    // this CTA's keys that carry the second pass's 16-bit prefix
+    uint32_t cand_n;
+    uint32_t xoff[kTopkCluster + 1];  // every rank's candidate count, as offsets
+    uint32_t all_key[kTopkCluster * kTopkCandCap];  // the cluster's candidates, rank by rank
+    uint8_t all_rank[kTopkCluster * kTopkCandCap];
     int32_t pick_pos[kTopkPickCap]; // this CTA's first picks (positions), in output order
     int32_t src_row[kTopkPickCap];  // their pool rows (page * 64 + slot), -1 for a bad page
 };
@@ -430,6 +436,97 @@ __global__ void __launch_bounds__(kTopkThreads) topk_gather_kernel(TopkParams p)
             }
             __syncthreads();  // pick[] and warp_sum[] are rewritten by the next pass
             tr.at(0x8220 + pass);
+            if (pass == 1 && staged) {
+                // After two bytes only a few keys still carry the prefix (about 30 per sequence of
+                // normally spread scores).  Each CTA offers its own; after one cluster barrier every
+                // CTA reads them all and finds the threshold key among them directly, instead of two
+                // more histogram passes.  If any CTA has more than kTopkCandCap of them (tie-heavy
+                // scores), every CTA sees it and the passes go on.
+                if (tid == 0) sm.cand_n = 0u;
+                __syncthreads();
+                auto offer = [&](uint32_t key, bool in) {  // whole warps call this
+                    const uint32_t bal = __ballot_sync(0xffffffffu, in);
+                    if (bal == 0u) return;
+                    uint32_t base = 0;
+                    if (lane == 0) base = atomicAdd(&sm.cand_n, (uint32_t)__popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (in) {
+                        const uint32_t slot = base + __popc(bal & lt);
+                        if (slot < (uint32_t)kTopkCandCap) sm.cand[slot] = key;
+                    }
+                };
+                if (!sm.list_overflow) {
+                    const uint32_t n = sm.wlist_n[warp];
+                    for (uint32_t j0 = 0; j0 < n; j0 += 32) {
+                        const uint32_t j = j0 + lane;
+                        const uint32_t key = j < n ? staged_keys[sm.wlist[warp][j] - lo] : 0u;
+                        offer(key, j < n && (key & mask) == prefix);
+                    }
+                } else {
+                    for (int e0 = wlo; e0 < whi; e0 += 128) {
+                        const int e = e0 + 4 * lane;
+                        uint32_t k4[4] = {0u, 0u, 0u, 0u};
+                        if (e < whi) topk_keys4(staged_keys, row, true, lo, e, k4);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) offer(k4[i], e + i < whi && (k4[i] & mask) == prefix);
+                    }
+                }
+                __syncthreads();
+                cluster_sync_all();  // every CTA's candidates are published
+                if (tid < 32) {  // one warp: lane q reads rank q's count, a scan makes the offsets
+                    uint32_t n = lane < kTopkCluster ? topk_ld_cluster(mapa_shared(smem_u32(&sm.cand_n), (uint32_t)lane))
+                                                     : 0u;
+                    if (n > (uint32_t)kTopkCandCap) n = 1u << 20;  // an overflow poisons the total
+                    uint32_t x = n;
+#pragma unroll
+                    for (int o = 1; o < kTopkCluster; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (lane < kTopkCluster) sm.xoff[lane + 1] = x;
+                    if (lane == 0) sm.xoff[0] = 0u;
+                }
+                __syncthreads();
+                const uint32_t total = sm.xoff[kTopkCluster];
+                if (total <= (uint32_t)(kTopkCluster * kTopkCandCap)) {
+                    if (tid < (int)total) {
+                        int q = 0;
+                        while (sm.xoff[q + 1] <= (uint32_t)tid) ++q;
+                        const uint32_t a = smem_u32(&sm.cand[tid - (int)sm.xoff[q]]);
+                        sm.all_key[tid] = topk_ld_cluster(mapa_shared(a, (uint32_t)q));
+                        sm.all_rank[tid] = (uint8_t)q;
+                    }
+                    cluster_arrive_relaxed();  // this CTA has read the others' shared memory
+                    __syncthreads();
+                    // the need-th largest candidate: fewer than `need` candidates above it, at least
+                    // `need` at or above it
+                    if (tid < (int)total) {
+                        const uint32_t mine = sm.all_key[tid];
+                        uint32_t gt = 0, ge = 0;
+                        for (uint32_t j = 0; j < total; ++j) {
+                            const uint32_t o = sm.all_key[j];
+                            gt += o > mine ? 1u : 0u;
+                            ge += o >= mine ? 1u : 0u;
+                        }
+                        if (gt < need && ge >= need) {
+                            sm.pick[0] = mine;
+                            sm.pick[1] = gt;
+                        }
+                    }
+                    __syncthreads();
+                    const uint32_t T = sm.pick[0];
+                    if (tid < (int)total) {
+                        const uint32_t key = sm.all_key[tid];
+                        if (key > T) atomicAdd(&sm.rank_gt[sm.all_rank[tid]], 1u);
+                        else if (key == T) atomicAdd(&sm.rank_eq[sm.all_rank[tid]], 1u);
+                    }
+                    need -= sm.pick[1];
+                    prefix = T;
+                    mask = 0xFFFFFFFFu;
+                    tr.at(0x8270);
+                    break;
+                }
+            }
         }
         if (tid < kTopkBins) {
 #pragma unroll

@@ -206,6 +206,7 @@ TOPK_STEPS = [("keys staged", 0x8201)] + [
     (f"pass {i}: {what}", tag + i) for i in range(4) for what, tag in (
         ("histogram counted", 0x8210), ("cluster barrier passed", 0x8240), ("cluster sum read", 0x8250),
         ("bin chosen", 0x8260), ("rank counts added", 0x8220))] + [
+    ("candidates exchanged, threshold found", 0x8270)] + [
     ("output offsets known", 0x8231), ("positions written", 0x8232), ("rows' pool offsets", 0x8233),
     ("rows copied", 0x8234)]
 
