@@ -331,6 +331,28 @@ def test_index_scores_e4m3_match_oracle(d_idx):
     assert mla.get_device_status() == (0, 0)
 
 
+def test_e4m3_nan_codes_give_nan_scores_that_rank_last():
+    """A token whose codes include S.1111.111 (NaN) scores NaN, as the oracle's decoding says,
+    and is picked only after every other token."""
+    sc = workloads.make_sparse_case("s", [200], k=8, d_idx=64, e4m3=True, seed=80)
+    codes = sc.idx_codes.clone()
+    bt = sc.case.block_table
+    bad = [3, 64, 150]
+    for t, c in zip(bad, (0x7F, 0xFF, 0x7F)):
+        codes[bt[0, t // 64], t % 64, 5] = c
+    d = _to_dev(sc)
+    scores = mla.index_scores_e4m3(d["q_idx"], codes.to(DEV), sc.idx_scale.to(DEV), d["bt"], d["sl"])
+    torch.cuda.synchronize()
+    g = scores.cpu().numpy()[0, :200]
+    ref = oracle.index_scores_e4m3(_np(sc.q_idx), codes.numpy(), sc.idx_scale.numpy(), bt.numpy(),
+                                   sc.case.seq_lens.numpy())[0]
+    assert np.array_equal(np.isnan(g), np.isnan(ref)) and sorted(np.where(np.isnan(g))[0]) == bad
+    si, _, _, sn = mla.topk_gather(scores, d["sl"], d["pool"], d["bt"], 199)
+    sel = si.cpu().numpy()[0, :int(sn[0])]
+    assert np.array_equal(sel, oracle.topk_row(g.astype(np.float64), 199))
+    assert set(bad) - set(sel.tolist()) == {150}  # of the three NaN tokens the two lowest are taken last
+
+
 def test_decode_sparse_with_an_e4m3_index_cache():
     k = 300
     sc = workloads.make_sparse_case("s", [0, 40, 700, 5000, 20000], k=k, shuffle=True, spare_pages=2, garbage="nan",
